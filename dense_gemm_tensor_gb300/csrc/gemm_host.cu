@@ -1,0 +1,306 @@
+// C-ABI entry points: argument checks, device checks, TMA tensor-map encoding,
+// variant selection and the persistent-grid launch. No allocation per call.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "dgt_gemm.h"
+#include "launch.h"
+
+namespace dgt {
+
+// Device status words: [0] first recorded failure (sticky), [1] epoch of the
+// most recently aborted launch. One copy per device that loads the library.
+__device__ uint32_t g_status_words[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s
+
+struct DeviceInfo {
+  int status;  // GEMM_OK or the reason this device cannot run the kernels
+  int sm_count;
+  uint32_t* status_words;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+std::atomic<uint32_t> g_epoch{1};
+std::atomic<uint64_t> g_launches{0};
+std::atomic<uint32_t> g_debug_flags{0};
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// Looks up (once per device) whether the current device is an sm_103 part,
+// its SM count and the device address of the status words.
+int current_device(const DeviceInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMM_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::call_once(g_dev_once[dev], [dev] {
+    DeviceInfo& d = g_dev[dev];
+    int major = 0, minor = 0;
+    d.status = GEMM_ERR_UNSUPPORTED_DEVICE;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    if (major != 10 || minor != 3) return;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_words) != cudaSuccess) {
+      cudaGetLastError();
+      d.status = GEMM_ERR_LAUNCH;
+      return;
+    }
+    d.status_words = static_cast<uint32_t*>(p);
+    d.status = GEMM_OK;
+  });
+  *out = &g_dev[dev];
+  return g_dev[dev].status;
+}
+
+// Device (or managed) memory of the current device?
+bool is_device_memory(const void* ptr) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeManaged) return true;
+  if (a.type != cudaMemoryTypeDevice) return false;
+  int dev = -1;
+  cudaGetDevice(&dev);
+  return a.device == dev;
+}
+
+// Byte range [lo, hi) touched by a rows x cols matrix with row pitch ld.
+void extent(const void* p, int64_t rows, int64_t cols, int64_t ld, int es, uintptr_t* lo, uintptr_t* hi) {
+  *lo = reinterpret_cast<uintptr_t>(p);
+  *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * es);
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// Largest power-of-two granularity in [es, 16] that divides the address and
+// the row pitch in bytes.
+int granularity(const void* p, int64_t ld, int es) {
+  const uint64_t v = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(p)) | static_cast<uint64_t>(ld * es);
+  int g = 16;
+  while (g > es && (v % g) != 0) g >>= 1;
+  return g;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+             void* C, int64_t ldc, int layout, void* stream_ptr) {
+  const int es = (kind == KIND_TF32) ? 4 : 2;
+  const int64_t kLim = (int64_t(1) << 31) - 1;
+  if (M < 0 || N < 0 || K < 0 || M > kLim || N > kLim || K > kLim) return GEMM_ERR_INVALID_VALUE;
+  if (layout != GEMM_B_ROW_MAJOR && layout != GEMM_B_K_MAJOR) return GEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_VALUE;
+  if (K > 0) {
+    if (A == nullptr || B == nullptr || lda < K) return GEMM_ERR_INVALID_VALUE;
+    if (ldb < (layout == GEMM_B_ROW_MAJOR ? N : K)) return GEMM_ERR_INVALID_VALUE;
+    if (lda > (int64_t(1) << 40) / es || ldb > (int64_t(1) << 40) / es) return GEMM_ERR_INVALID_VALUE;
+  }
+  if (ldc > (int64_t(1) << 40) / es) return GEMM_ERR_INVALID_VALUE;
+  const int64_t tiles_m = (M + 127) / 128, tiles_n = (N + 255) / 256;
+  if (tiles_m * tiles_n > kLim) return GEMM_ERR_INVALID_VALUE;
+
+  auto mis = [es](const void* p) { return (reinterpret_cast<uintptr_t>(p) % es) != 0; };
+  if (mis(C) || (K > 0 && (mis(A) || mis(B)))) return GEMM_ERR_MISALIGNED;
+
+  const DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+
+  uintptr_t c0, c1;
+  extent(C, M, N, ldc, es, &c0, &c1);
+  if (!is_device_memory(C)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  if (K == 0) {
+    cudaError_t e = launch_fill_zero(C, ldc, int(M), int(N), es, stream, dev->sm_count);
+    if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return GEMM_OK;
+  }
+
+  uintptr_t a0, a1, b0, b1;
+  extent(A, M, K, lda, es, &a0, &a1);
+  if (layout == GEMM_B_ROW_MAJOR)
+    extent(B, K, N, ldb, es, &b0, &b1);
+  else
+    extent(B, N, K, ldb, es, &b0, &b1);
+  if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return GEMM_ERR_INVALID_VALUE;
+  if (!is_device_memory(A) || !is_device_memory(B)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+
+  LaunchPlan L;
+  memset(&L, 0, sizeof(L));
+  GemmParams& p = L.p;
+  p.M = int(M);
+  p.N = int(N);
+  p.K = int(K);
+  p.tiles_m = int(tiles_m);
+  p.tiles_n = int(tiles_n);
+  p.num_tiles = int(tiles_m * tiles_n);
+  p.num_kb = int((K * es + 127) / 128);
+  p.raster = 8;
+  p.A = A;
+  p.lda = lda;
+  p.B = B;
+  p.ldb = ldb;
+  p.C = C;
+  p.ldc = ldc;
+  const int ga = granularity(A, lda, es), gb = granularity(B, ldb, es);
+  p.a_tma = ga == 16;
+  p.b_tma = gb == 16;
+  p.copy_bytes = 16;
+  if (!p.a_tma) p.copy_bytes = ga;
+  if (!p.b_tma && gb < p.copy_bytes) p.copy_bytes = gb;
+  p.c_vec = granularity(C, ldc, es) == 16;
+  p.status = dev->status_words;
+  uint32_t ep = g_epoch.fetch_add(1, std::memory_order_relaxed);
+  if (ep == 0) ep = g_epoch.fetch_add(1, std::memory_order_relaxed);
+  p.epoch = ep;
+  p.debug = g_debug_flags.load(std::memory_order_relaxed);
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+
+  const CUtensorMapDataType dt = kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint32_t bk = 128 / es;  // K elements per 128-byte row
+  if (p.a_tma && !encode_2d(&L.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda) * es, bk, 128))
+    return GEMM_ERR_DRIVER;
+  if (p.b_tma) {
+    bool ok;
+    if (layout == GEMM_B_K_MAJOR)
+      ok = encode_2d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, bk, 256);
+    else
+      ok = encode_2d(&L.tmB, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, 128 / es, bk);
+    if (!ok) return GEMM_ERR_DRIVER;
+  }
+  L.b_kmajor = layout == GEMM_B_K_MAJOR;
+  L.grid = p.num_tiles < dev->sm_count ? p.num_tiles : dev->sm_count;
+  L.threads = (p.a_tma && p.b_tma) ? 192 : 320;
+  L.stream = stream;
+
+  cudaError_t e = kind == KIND_TF32 ? launch_tf32(L) : kind == KIND_BF16 ? launch_bf16(L) : launch_f16(L);
+  if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return GEMM_OK;
+}
+
+}  // namespace
+
+cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count) {
+  const long long total = static_cast<long long>(M) * N;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 4LL * sm_count) blocks = 4LL * sm_count;
+  if (es == 4)
+    fill_zero_kernel<4><<<int(blocks), 256, 0, stream>>>(C, ldc, M, N);
+  else
+    fill_zero_kernel<2><<<int(blocks), 256, 0, stream>>>(C, ldc, M, N);
+  return cudaGetLastError();
+}
+
+}  // namespace dgt
+
+extern "C" {
+
+int gemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
+              int64_t ldc, int layout, void* stream) {
+  return dgt::run_gemm(dgt::KIND_TF32, M, N, K, A, lda, B, ldb, C, ldc, layout, stream);
+}
+
+int gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+             uint16_t* C, int64_t ldc, int layout, void* stream) {
+  return dgt::run_gemm(dgt::KIND_F16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream);
+}
+
+int gemm_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+              uint16_t* C, int64_t ldc, int layout, void* stream) {
+  return dgt::run_gemm(dgt::KIND_BF16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream);
+}
+
+const char* gemm_status_string(int status) {
+  switch (status) {
+    case GEMM_OK: return "success";
+    case GEMM_ERR_INVALID_VALUE: return "invalid argument (size, leading dimension, layout, NULL or overlap)";
+    case GEMM_ERR_MISALIGNED: return "pointer not aligned to its element size";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (sm_103)";
+    case GEMM_ERR_LAUNCH: return "CUDA launch or synchronisation failed";
+    case GEMM_ERR_NOT_DEVICE_MEMORY: return "pointer is not device memory of the current device";
+    case GEMM_ERR_DRIVER: return "tensor-map encoding failed in the CUDA driver";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel exceeded its wait time limit and gave up";
+    default: return "unknown status";
+  }
+}
+
+int gemm_get_device_status(void* stream, uint32_t* out) {
+  if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
+  const dgt::DeviceInfo* dev = nullptr;
+  int st = dgt::current_device(&dev);
+  if (st != GEMM_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_LAUNCH;
+  uint32_t w[2] = {0, 0};
+  if (cudaMemcpy(w, dev->status_words, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_LAUNCH;
+  *out = w[0];
+  return w[0] ? GEMM_ERR_DEVICE_TIMEOUT : GEMM_OK;
+}
+
+int gemm_reset_device_status(void) {
+  const dgt::DeviceInfo* dev = nullptr;
+  int st = dgt::current_device(&dev);
+  if (st != GEMM_OK) return st;
+  if (cudaMemset(dev->status_words, 0, 2 * sizeof(uint32_t)) != cudaSuccess) return GEMM_ERR_LAUNCH;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_LAUNCH;
+  return GEMM_OK;
+}
+
+int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns) {
+  dgt::g_debug_flags.store(flags);
+  dgt::g_wait_limit_ns.store(wait_limit_ns ? wait_limit_ns : dgt::kDefaultWaitLimitNs);
+  return GEMM_OK;
+}
+
+uint64_t gemm_launch_count(void) { return dgt::g_launches.load(); }
+
+}  // extern "C"

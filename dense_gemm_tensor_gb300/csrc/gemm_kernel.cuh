@@ -1,0 +1,532 @@
+// Persistent, warp-specialised dense GEMM for sm_103a:  C (M x N) = A (M x K) . B (K x N).
+//
+// The method is the dense matrix product of the TF32 and FP16/BF16 GEMM pages
+// ("sgemm tf32 - beating cuBLAS" and "hgemm - beating cuBLAS"): block tiling
+// with operands staged through shared memory, a pipelined k-loop, tensor-core
+// MMA with fp32 accumulation, grid-swizzled tile order for L2 reuse, and an
+// epilogue that converts the fp32 accumulator to the output type with
+// round-to-nearest-even. Here each of those steps is a Blackwell unit:
+//
+//   * one CTA per SM loops over output tiles of BM x BN = 128 x 256 in a
+//     banded order (the pages' grid swizzle, generalised to ragged grids);
+//   * warp 4 (one thread) streams A and B boxes with TMA into a 4-stage ring
+//     of 128-byte-swizzled shared-memory tiles (the hardware swizzle replaces
+//     the pages' hand-derived XOR layouts); for an operand whose rows TMA
+//     cannot address (row pitch not a multiple of 16 bytes) warps 6-9 copy it
+//     with cp.async into the same swizzled image;
+//   * warp 5 (one thread) issues tcgen05.mma 128 x 256 x (32 bytes of K) with
+//     the accumulator in tensor memory, two accumulators of 256 columns so the
+//     epilogue of one tile overlaps the k-loop of the next;
+//   * warps 0-3 read the accumulator with tcgen05.ld (warp w owns TMEM lanes
+//     32w..32w+31 = tile rows), convert and store C.
+//
+// Every wait on an mbarrier is bounded: past the launch's time limit the
+// waiting thread records a timeout in the device status word and the CTA
+// winds down (in-flight copies and MMAs are drained, TMEM is freed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace dgt {
+
+enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_TF32 = 2 };
+
+template <int KIND>
+struct KindTraits;
+template <>
+struct KindTraits<KIND_F16> {
+  using T = __half;
+  static constexpr uint32_t fmt = 0;  // instruction-descriptor operand format F16
+};
+template <>
+struct KindTraits<KIND_BF16> {
+  using T = __nv_bfloat16;
+  static constexpr uint32_t fmt = 1;  // BF16
+};
+template <>
+struct KindTraits<KIND_TF32> {
+  using T = float;
+  static constexpr uint32_t fmt = 2;  // TF32
+};
+
+// Status word codes (device status[0]); status[1] holds the epoch of the last aborted launch.
+enum : uint32_t {
+  STATUS_TIMEOUT = 1u,
+  ROLE_PRODUCER = 1u << 4,
+  ROLE_MMA = 2u << 4,
+  ROLE_EPILOGUE = 3u << 4,
+  ROLE_COPY = 4u << 4,
+  ROLE_TEARDOWN = 5u << 4,
+};
+enum : uint32_t { DEBUG_STALL_PRODUCER = 1u };
+
+struct GemmParams {
+  int M, N, K;
+  int tiles_m, tiles_n, num_tiles, num_kb;
+  int raster;  // band height (in tiles along M) of the tile order
+  const void* A;
+  long long lda;
+  const void* B;
+  long long ldb;
+  void* C;
+  long long ldc;
+  int a_tma, b_tma;  // operand loaded by TMA (1) or by the copy warps (0)
+  int copy_bytes;    // copy-warp granularity in bytes: 16, 8, 4 or 2
+  int c_vec;         // C base and row pitch allow 16-byte stores
+  uint32_t* status;  // device status words [2]
+  uint32_t epoch;    // unique per launch
+  uint32_t debug;
+  unsigned long long wait_limit_ns;
+};
+
+template <int KIND, bool B_KMAJOR>
+struct Cfg {
+  using T = typename KindTraits<KIND>::T;
+  static constexpr int ES = sizeof(T);
+  static constexpr int BM = 128;
+  static constexpr int BN = 256;
+  static constexpr int BK = 128 / ES;       // one 128-byte swizzle row of K per stage
+  static constexpr int UK = 32 / ES;        // K of one tcgen05.mma (16 for 16-bit, 8 for tf32)
+  static constexpr int KSTEPS = BK / UK;    // MMAs per stage
+  static constexpr int STAGES = 4;
+  static constexpr int A_BYTES = BM * 128;  // 16 KB
+  static constexpr int B_BYTES = BN * 128;  // 32 KB
+  static constexpr int BOXN = 128 / ES;     // MN-major B: N elements per 128-byte box row
+  static constexpr int NBOX = BN / BOXN;    // MN-major B: boxes per stage
+  static constexpr int BOX_BYTES = BK * 128;
+  static constexpr int ACC_COLS = BN;       // fp32 accumulator columns of one buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+  static constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
+  static constexpr int THREADS_TMA = 192;   // 4 epilogue + producer + MMA warps
+  static constexpr int THREADS_COPY = 320;  // + 4 copy warps
+  static constexpr int COPY_LAG = 2;        // stages a copy warp keeps in flight before signalling
+  static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
+
+  // Instruction descriptor: D fp32, A/B format, A K-major, B K- or MN-major, N, M.
+  static constexpr uint32_t IDESC = (1u << 4) | (KindTraits<KIND>::fmt << 7) | (KindTraits<KIND>::fmt << 10) |
+                                    ((B_KMAJOR ? 0u : 1u) << 16) | (uint32_t(BN >> 3) << 17) |
+                                    (uint32_t(BM >> 4) << 24);
+};
+
+// Linear work id -> output tile. Tiles go in bands of `raster` tile-rows: down
+// the band's rows first, then across N, band after band. A band's B tiles and
+// its A row-tiles stay in L2 while the band is worked on.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
+  const int band = p.raster * p.tiles_n;
+  const int g = t / band;
+  const int first_m = g * p.raster;
+  const int rows = min(p.raster, p.tiles_m - first_m);
+  const int r = t - g * band;
+  mb = first_m + r % rows;
+  nb = r / rows;
+}
+
+static __device__ __noinline__ void record_timeout(const GemmParams& p, uint32_t code) {
+  atomicCAS(p.status, 0u, code | STATUS_TIMEOUT | ((blockIdx.x & 0xFFFFu) << 16));
+  atomicExch(p.status + 1, p.epoch);
+  __threadfence();
+}
+
+// Bounded wait for the phase of `bar` with `parity`. Returns false when this
+// launch has been aborted (by this thread's own time limit or another's).
+__device__ __forceinline__ bool wait_phase(const GemmParams& p, uint32_t bar, uint32_t parity, uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (ld_volatile_u32(p.status + 1) == p.epoch) return false;
+      if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+        record_timeout(p, code);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used while draining after an abort).
+__device__ __forceinline__ bool wait_phase_drain(const GemmParams& p, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+      record_timeout(p, ROLE_TEARDOWN);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Warp-uniform version: lane 0 waits, the outcome is broadcast.
+__device__ __forceinline__ bool warp_wait_phase(const GemmParams& p, uint32_t bar, uint32_t parity, uint32_t code) {
+  uint32_t ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_phase(p, bar, parity, code) ? 1u : 0u;
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// ------------------------------------------------------------------ copy warps
+// Copy `bytes` (<= 16, chunk never crosses a 16-byte unit) from global to a
+// swizzled shared-memory position; `valid` bytes come from memory, the rest
+// are zero. Granularity >= 4 uses cp.async, 2 uses a plain load and store.
+__device__ __forceinline__ void copy_chunk(uint32_t dst, const uint8_t* src, int gran, int valid) {
+  if (gran == 16) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid) : "memory");
+  } else if (gran == 8) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(valid) : "memory");
+  } else if (gran == 4) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid) : "memory");
+  } else {
+    uint16_t v = 0;
+    if (valid >= 2) v = *reinterpret_cast<const uint16_t*>(src);
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(dst), "h"(v) : "memory");
+  }
+}
+
+// One K-major operand tile: `rows` rows (M or N) of 128 bytes along K.
+// Row r of the tile is global row (row0 + r), bytes from k0 * ES.
+template <int ES>
+__device__ __forceinline__ void copy_kmajor_tile(uint32_t sdst, const uint8_t* base, long long ld_bytes,
+                                                 int rows, int row0, int row_lim, int k0, int K, int gran,
+                                                 int tid) {
+  const int per_row = 128 / gran;
+  const int total = rows * per_row;
+  const long long kbytes_lim = static_cast<long long>(K) * ES;
+  for (int c = tid; c < total; c += 128) {
+    const int r = c / per_row;
+    const int byte = (c - r * per_row) * gran;
+    const uint32_t dst = sdst + r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15));
+    const int grow = row0 + r;
+    const long long gk = static_cast<long long>(k0) * ES + byte;
+    int valid = 0;
+    if (grow < row_lim && gk < kbytes_lim) valid = (kbytes_lim - gk < gran) ? static_cast<int>(kbytes_lim - gk) : gran;
+    const uint8_t* src = valid ? base + grow * ld_bytes + gk : base;
+    copy_chunk(dst, src, gran, valid);
+  }
+}
+
+// One MN-major B tile: NBOX boxes, each BK rows (K) of 128 bytes along N.
+template <int ES, int BK, int NBOX, int BOX_BYTES>
+__device__ __forceinline__ void copy_mnmajor_tile(uint32_t sdst, const uint8_t* base, long long ld_bytes, int n0,
+                                                  int N, int k0, int K, int gran, int tid) {
+  const int per_row = 128 / gran;
+  const int total = NBOX * BK * per_row;
+  const long long nbytes_lim = static_cast<long long>(N) * ES;
+  for (int c = tid; c < total; c += 128) {
+    const int row = c / per_row;  // box * BK + k
+    const int byte = (c - row * per_row) * gran;
+    const int box = row / BK;
+    const int k = row - box * BK;
+    const uint32_t dst = sdst + box * BOX_BYTES + k * 128 + ((((byte >> 4) ^ (k & 7)) << 4) | (byte & 15));
+    const int gk = k0 + k;
+    const long long gn = static_cast<long long>(n0) * ES + box * 128 + byte;
+    int valid = 0;
+    if (gk < K && gn < nbytes_lim) valid = (nbytes_lim - gn < gran) ? static_cast<int>(nbytes_lim - gn) : gran;
+    const uint8_t* src = valid ? base + gk * ld_bytes + gn : base;
+    copy_chunk(dst, src, gran, valid);
+  }
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Generic-proxy writes to shared memory become visible to tcgen05.mma (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ epilogue helpers
+template <int KIND>
+__device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
+  const float a = __uint_as_float(lo), b = __uint_as_float(hi);
+  if constexpr (KIND == KIND_BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void store_one(void* C, long long idx, uint32_t bits) {
+  if constexpr (KIND == KIND_TF32) {
+    reinterpret_cast<uint32_t*>(C)[idx] = bits;
+  } else if constexpr (KIND == KIND_BF16) {
+    reinterpret_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(__uint_as_float(bits));
+  } else {
+    reinterpret_cast<__half*>(C)[idx] = __float2half_rn(__uint_as_float(bits));
+  }
+}
+
+// 32 accumulator columns of one row -> C[row][col0 .. col0+31].
+template <int KIND>
+__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, int col0, const uint32_t (&r)[32]) {
+  if (row >= p.M || col0 >= p.N) return;
+  const long long idx0 = static_cast<long long>(row) * p.ldc + col0;
+  if (p.c_vec && col0 + 32 <= p.N) {
+    if constexpr (KIND == KIND_TF32) {
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(p.C) + idx0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dst[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.C) + idx0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_uint4(pack2<KIND>(r[8 * q], r[8 * q + 1]), pack2<KIND>(r[8 * q + 2], r[8 * q + 3]),
+                            pack2<KIND>(r[8 * q + 4], r[8 * q + 5]), pack2<KIND>(r[8 * q + 6], r[8 * q + 7]));
+    }
+  } else {
+    const int lim = min(32, p.N - col0);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < lim) store_one<KIND>(p.C, idx0 + j, r[j]);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int KIND, bool B_KMAJOR>
+__global__ void __launch_bounds__(320, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p) {
+  using Cf = Cfg<KIND, B_KMAJOR>;
+  constexpr int S = Cf::STAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sptr = smem_raw + (sbase - raw);
+  const uint32_t sA = sbase;
+  const uint32_t sB = sbase + S * Cf::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sptr + S * (Cf::A_BYTES + Cf::B_BYTES));
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * S;
+  const uint32_t accf0 = empty0 + 8 * S;
+  const uint32_t acce0 = accf0 + 16;
+  const uint32_t drain_bar = acce0 + 16;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + Cf::NUM_BARS);
+  volatile int* issued_slot = reinterpret_cast<volatile int*>(bars + Cf::NUM_BARS) + 1;
+  volatile int* consumed_slot = reinterpret_cast<volatile int*>(bars + Cf::NUM_BARS) + 2;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool has_copy = !(p.a_tma && p.b_tma);
+  const uint32_t full_count = 1u + (has_copy ? 4u : 0u);
+
+  if (warp == 4 && lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, full_count);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 4);
+    }
+    mbar_init(drain_bar, 1);
+    *issued_slot = 0;
+    *consumed_slot = 0;
+    fence_mbar_init();
+    if (p.a_tma) tma_prefetch_desc(&tmA);
+    if (p.b_tma) tma_prefetch_desc(&tmB);
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), Cf::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && !(p.debug & DEBUG_STALL_PRODUCER)) {
+      const uint32_t tx = (p.a_tma ? Cf::A_BYTES : 0) + (p.b_tma ? Cf::B_BYTES : 0);
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, t, mb, nb);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!wait_phase(p, empty0 + 8 * s, ph ^ 1, ROLE_PRODUCER | (s << 8))) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * s;
+          mbar_arrive_expect_tx(fb, tx);
+          if (p.a_tma) tma_load_2d(sA + s * Cf::A_BYTES, &tmA, fb, kb * Cf::BK, mb * Cf::BM);
+          if (p.b_tma) {
+            if constexpr (B_KMAJOR) {
+              tma_load_2d(sB + s * Cf::B_BYTES, &tmB, fb, kb * Cf::BK, nb * Cf::BN);
+            } else {
+#pragma unroll
+              for (int j = 0; j < Cf::NBOX; ++j)
+                tma_load_2d(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, nb * Cf::BN + j * Cf::BOXN,
+                            kb * Cf::BK);
+            }
+          }
+        }
+      }
+      *issued_slot = it;
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tc) {
+        const int b = tc & 1;
+        const uint32_t use = (tc >> 1) & 1;
+        if (!wait_phase(p, acce0 + 8 * b, use ^ 1, ROLE_MMA | (0x80u << 8))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * Cf::ACC_COLS;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!wait_phase(p, full0 + 8 * s, ph, ROLE_MMA | (s << 8))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sA + s * Cf::A_BYTES;
+          const uint32_t b_addr = sB + s * Cf::B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
+            const uint64_t ad = sdesc_sw128(a_addr + kk * 32, 16, 1024);
+            uint64_t bd;
+            if constexpr (B_KMAJOR)
+              bd = sdesc_sw128(b_addr + kk * 32, 16, 1024);
+            else
+              bd = sdesc_sw128(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, 1024);
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            if constexpr (KIND == KIND_TF32)
+              mma_tf32(d, ad, bd, Cf::IDESC, acc);
+            else
+              mma_f16(d, ad, bd, Cf::IDESC, acc);
+          }
+          mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs have read it
+        }
+        if (!ok) break;
+        mma_commit(accf0 + 8 * b);  // accumulator ready for the epilogue
+      }
+      *consumed_slot = it;
+      // wait for every MMA this thread issued (normally already complete)
+      mma_commit(drain_bar);
+      wait_phase_drain(p, drain_bar, 0);
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- epilogue
+    int tc = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tc) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int b = tc & 1;
+      const uint32_t use = (tc >> 1) & 1;
+      if (!warp_wait_phase(p, accf0 + 8 * b, use, ROLE_EPILOGUE | (b << 8))) break;
+      tc_fence_after();
+      const int row = mb * Cf::BM + warp * 32 + lane;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
+      const int ncols = min(Cf::BN, p.N - nb * Cf::BN);
+#pragma unroll 1
+      for (int c = 0; c < Cf::BN / 32; ++c) {
+        if (c * 32 >= ncols) break;  // warp-uniform
+        uint32_t r[32];
+        __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane stores
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_wait_ld();
+        store_row_chunk<KIND>(p, row, nb * Cf::BN + c * 32, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * b);
+    }
+  } else {
+    // ---------------------------------------------------------------- copy warps (6-9)
+    const int ctid = threadIdx.x - 6 * 32;  // 0..127
+    const uint8_t* Ab = static_cast<const uint8_t*>(p.A);
+    const uint8_t* Bb = static_cast<const uint8_t*>(p.B);
+    const long long lda_b = p.lda * Cf::ES, ldb_b = p.ldb * Cf::ES;
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const int s = it % S;
+        const uint32_t ph = (it / S) & 1;
+        if (!warp_wait_phase(p, empty0 + 8 * s, ph ^ 1, ROLE_COPY | (s << 8))) {
+          ok = false;
+          break;
+        }
+        if (!p.a_tma)
+          copy_kmajor_tile<Cf::ES>(sA + s * Cf::A_BYTES, Ab, lda_b, Cf::BM, mb * Cf::BM, p.M, kb * Cf::BK, p.K,
+                                   p.copy_bytes, ctid);
+        if (!p.b_tma) {
+          if constexpr (B_KMAJOR)
+            copy_kmajor_tile<Cf::ES>(sB + s * Cf::B_BYTES, Bb, ldb_b, Cf::BN, nb * Cf::BN, p.N, kb * Cf::BK, p.K,
+                                     p.copy_bytes, ctid);
+          else
+            copy_mnmajor_tile<Cf::ES, Cf::BK, Cf::NBOX, Cf::BOX_BYTES>(sB + s * Cf::B_BYTES, Bb, ldb_b,
+                                                                        nb * Cf::BN, p.N, kb * Cf::BK, p.K,
+                                                                        p.copy_bytes, ctid);
+        }
+        cp_async_commit();
+        if (it >= Cf::COPY_LAG) {
+          // the copies of stage (it - LAG) have landed: publish them to the MMA
+          cp_async_wait<Cf::COPY_LAG>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full0 + 8 * ((it - Cf::COPY_LAG) % S));
+        }
+      }
+    }
+    // publish the last stages (also on abort: nothing may stay in flight)
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (ok && lane == 0) {
+      for (int j = max(0, it - Cf::COPY_LAG); j < it; ++j) mbar_arrive(full0 + 8 * (j % S));
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && ld_volatile_u32(p.status + 1) == p.epoch) {
+    // aborted: let every TMA load that was issued but not consumed land first
+    const int issued = *issued_slot, consumed = *consumed_slot;
+    if (p.a_tma || p.b_tma)
+      for (int j = consumed; j < issued; ++j)
+        if (!wait_phase_drain(p, full0 + 8 * (j % S), (j / S) & 1)) break;
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cf::TMEM_COLS);
+  }
+}
+
+// Writes C = 0 (the K = 0 product) for any layout.
+template <int ES>
+__global__ void fill_zero_kernel(void* C, long long ldc, int M, int N) {
+  const long long total = static_cast<long long>(M) * N;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / N, c = i - r * N;
+    if constexpr (ES == 4)
+      reinterpret_cast<uint32_t*>(C)[r * ldc + c] = 0u;
+    else
+      reinterpret_cast<uint16_t*>(C)[r * ldc + c] = 0;
+  }
+}
+
+}  // namespace dgt

@@ -1,0 +1,195 @@
+"""ctypes binding to ``libdgt_gemm.so``: argument marshalling only.
+
+The functions ``gemm_tf32``, ``gemm_f16`` and ``gemm_bf16`` have the names
+and arguments of the C interface (``include/dgt_gemm.h``) and take raw device
+pointers. ``matmul`` takes torch CUDA tensors and derives sizes, leading
+dimensions and the current stream from them; ``matmul_from_host`` is the
+end-to-end call for operands held in (pinned) host memory. Every step of the
+product runs in the library's CUDA kernels; there is no other code path, and
+a missing or unloadable library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdgt_gemm.so")
+
+GEMM_B_ROW_MAJOR = 0
+GEMM_B_K_MAJOR = 1
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_VALUE = 1
+GEMM_ERR_MISALIGNED = 2
+GEMM_ERR_UNSUPPORTED_DEVICE = 3
+GEMM_ERR_LAUNCH = 4
+GEMM_ERR_NOT_DEVICE_MEMORY = 5
+GEMM_ERR_DRIVER = 6
+GEMM_ERR_DEVICE_TIMEOUT = 7
+
+# Every symbol the C header declares.
+EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_get_device_status",
+           "gemm_reset_device_status", "gemm_set_debug", "gemm_launch_count")
+
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} (code {code})")
+        self.code = code
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with dense_gemm_tensor_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    i64, vp, u32, u64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64
+    for name in ("gemm_tf32", "gemm_f16", "gemm_bf16"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, vp]
+        fn.restype = ctypes.c_int
+    lib.gemm_status_string.argtypes = [ctypes.c_int]
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_get_device_status.argtypes = [vp, ctypes.POINTER(u32)]
+    lib.gemm_get_device_status.restype = ctypes.c_int
+    lib.gemm_reset_device_status.argtypes = []
+    lib.gemm_reset_device_status.restype = ctypes.c_int
+    lib.gemm_set_debug.argtypes = [u32, u64]
+    lib.gemm_set_debug.restype = ctypes.c_int
+    lib.gemm_launch_count.argtypes = []
+    lib.gemm_launch_count.restype = u64
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().gemm_status_string(int(code)).decode()
+
+
+def _call(name, M, N, K, A, lda, B, ldb, C, ldc, layout, stream):
+    return getattr(load(), name)(M, N, K, A, lda, B, ldb, C, ldc, layout, stream)
+
+
+def gemm_tf32(M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_MAJOR, stream=None) -> int:
+    """C = A . B, fp32 operands read as TF32; raw device pointers (ints)."""
+    return _call("gemm_tf32", M, N, K, A, lda, B, ldb, C, ldc, layout, stream)
+
+
+def gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_MAJOR, stream=None) -> int:
+    """C = A . B with IEEE half operands and output; raw device pointers."""
+    return _call("gemm_f16", M, N, K, A, lda, B, ldb, C, ldc, layout, stream)
+
+
+def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_MAJOR, stream=None) -> int:
+    """C = A . B with bfloat16 operands and output; raw device pointers."""
+    return _call("gemm_bf16", M, N, K, A, lda, B, ldb, C, ldc, layout, stream)
+
+
+_BY_DTYPE = {torch.float32: "gemm_tf32", torch.float16: "gemm_f16", torch.bfloat16: "gemm_bf16"}
+
+
+def _rows(t: torch.Tensor, what: str) -> int:
+    """Leading dimension of a 2-D tensor with unit column stride."""
+    if t.dim() != 2:
+        raise ValueError(f"{what} must be 2-D")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{what} must have unit stride along its rows")
+    return max(t.stride(0), t.shape[1]) if t.shape[0] > 1 else t.shape[1]
+
+
+def matmul(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, layout: int = GEMM_B_ROW_MAJOR,
+           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """C = A . B on the current CUDA device.
+
+    ``A``: M x K. ``B``: K x N for ``layout=GEMM_B_ROW_MAJOR``, or N x K (B
+    transposed) for ``layout=GEMM_B_K_MAJOR``. Rows may be padded (stride(0) >
+    row length) but elements along a row must be contiguous. The dtype selects
+    the entry point: float32 -> gemm_tf32, float16 -> gemm_f16, bfloat16 ->
+    gemm_bf16. ``out`` (M x N, same dtype) may have padded rows too.
+    """
+    if A.dtype not in _BY_DTYPE or B.dtype != A.dtype:
+        raise TypeError("A and B must both be float32, float16 or bfloat16")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    M, K = A.shape
+    if layout == GEMM_B_ROW_MAJOR:
+        if B.shape[0] != K:
+            raise ValueError("B must be K x N")
+        N = B.shape[1]
+    else:
+        if B.shape[1] != K:
+            raise ValueError("B must be N x K for the K-major layout")
+        N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    elif out.shape != (M, N) or out.dtype != A.dtype:
+        raise ValueError("out must be M x N with the operands' dtype")
+    s = stream if stream is not None else torch.cuda.current_stream(A.device)
+    code = _call(_BY_DTYPE[A.dtype], M, N, K, A.data_ptr() or None, _rows(A, "A"), B.data_ptr() or None,
+                 _rows(B, "B"), out.data_ptr() or None, _rows(out, "out"), layout, s.cuda_stream)
+    if code != GEMM_OK:
+        raise GemmError(code, _BY_DTYPE[A.dtype])
+    return out
+
+
+def matmul_from_host(A_host: torch.Tensor, B_host: torch.Tensor, *, layout: int = GEMM_B_ROW_MAJOR,
+                     device: torch.device | str = "cuda", stream: torch.cuda.Stream | None = None,
+                     buffers: dict | None = None) -> torch.Tensor:
+    """End-to-end product of host operands: copy A and B to the device, run
+    the kernel, copy C back into a pinned host tensor, and synchronise.
+
+    ``buffers`` (optional, reused across calls) caches the device and pinned
+    host buffers so repeated calls do not allocate.
+    """
+    buffers = {} if buffers is None else buffers
+    dev = torch.device(device)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    key = (A_host.shape, B_host.shape, A_host.dtype, layout)
+    if buffers.get("key") != key:
+        M = A_host.shape[0]
+        N = B_host.shape[1] if layout == GEMM_B_ROW_MAJOR else B_host.shape[0]
+        buffers.update(key=key,
+                       a=torch.empty(A_host.shape, dtype=A_host.dtype, device=dev),
+                       b=torch.empty(B_host.shape, dtype=B_host.dtype, device=dev),
+                       c=torch.empty((M, N), dtype=A_host.dtype, device=dev),
+                       c_host=torch.empty((M, N), dtype=A_host.dtype, pin_memory=True))
+    with torch.cuda.stream(s):
+        buffers["a"].copy_(A_host, non_blocking=True)
+        buffers["b"].copy_(B_host, non_blocking=True)
+        matmul(buffers["a"], buffers["b"], buffers["c"], layout=layout, stream=s)
+        buffers["c_host"].copy_(buffers["c"], non_blocking=True)
+    s.synchronize()
+    return buffers["c_host"]
+
+
+def device_status(stream: torch.cuda.Stream | None = None) -> int:
+    """Synchronise and read the device status word (0 = no kernel gave up)."""
+    out = ctypes.c_uint32(0)
+    s = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    code = load().gemm_get_device_status(s, ctypes.byref(out))
+    if code not in (GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT):
+        raise GemmError(code, "gemm_get_device_status")
+    return int(out.value)
+
+
+def reset_device_status() -> None:
+    code = load().gemm_reset_device_status()
+    if code != GEMM_OK:
+        raise GemmError(code, "gemm_reset_device_status")
+
+
+def set_debug(flags: int = 0, wait_limit_ns: int = 0) -> None:
+    load().gemm_set_debug(flags, wait_limit_ns)
+
+
+def launch_count() -> int:
+    return int(load().gemm_launch_count())

@@ -1,0 +1,120 @@
+/*
+ * dgt_gemm.h -- C interface of the GB300 (sm_103a) dense GEMM library.
+ *
+ *   C (M x N) = A (M x K) . B (K x N)
+ *
+ * The operation is the dense matrix product of the TF32 and FP16/BF16 GEMM
+ * pages: "sgemm tf32 - beating cuBLAS" (section 0: an M x K by K x N product
+ * with TF32 tensor-core inputs, fp32 in and out) and "hgemm - beating cuBLAS"
+ * (section 0: FP16/BF16 inputs with fp32 accumulation; section 1's epilogue
+ * rounds the fp32 result to the input type with round-to-nearest-even). Their
+ * kernels take (A, B, C, m, n, k) with dense row-major matrices and no
+ * alpha/beta; this interface adds leading dimensions, a layout flag for B and
+ * a CUDA stream.
+ *
+ * Layouts (element indices, not bytes):
+ *   A           row-major M x K:   A[i][k] = A[i * lda + k],  lda >= K
+ *   B, layout 0 row-major K x N:   B[k][j] = B[k * ldb + j],  ldb >= N
+ *   B, layout 1 K-major (B^T given as N x K): B[k][j] = B[j * ldb + k], ldb >= K
+ *   C           row-major M x N:   C[i][j] = C[i * ldc + j],  ldc >= N
+ *
+ * Arithmetic:
+ *   gemm_tf32: fp32 operands are read by the tensor core as TF32 (the low 13
+ *              mantissa bits are not used); fp32 accumulation; fp32 C.
+ *   gemm_f16 / gemm_bf16: IEEE binary16 / bfloat16 operands (passed as their
+ *              16-bit patterns); fp32 accumulation; C rounded to the input
+ *              type with round-to-nearest-even (IEEE overflow to +-inf).
+ *   The order of the fp32 additions is unspecified; results are deterministic
+ *   run to run (no atomics).
+ *
+ * Ownership and memory: every pointer is device memory (or managed memory) of
+ * the current CUDA device, owned by the caller. The library allocates nothing
+ * per call; it keeps, per device, two status words in its own module memory.
+ * C is fully overwritten and must not overlap A or B. Elements beyond the
+ * logical row length (columns >= K, >= N) are never read or written.
+ *
+ * Degenerate shapes: M = 0 or N = 0 does nothing; K = 0 writes C = 0.
+ *
+ * Asynchrony and errors: each call enqueues its work on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) and returns at once. The
+ * return value reports argument and launch errors only; a fault during
+ * execution surfaces at the next synchronisation of the stream, and a kernel
+ * that gave up waiting records it in the device status word
+ * (gemm_get_device_status). The calls are safe to make from several host
+ * threads.
+ *
+ * Any base address and leading dimension that keeps elements aligned to
+ * their size is accepted. Rows whose byte pitch is a multiple of 16 (and 16-byte
+ * aligned bases) are streamed with TMA; other operands are copied by the
+ * kernel's own copy warps, which is slower but gives the same results.
+ */
+#ifndef DGT_GEMM_H
+#define DGT_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* B layout flag */
+#define GEMM_B_ROW_MAJOR 0 /* B is K x N, row-major */
+#define GEMM_B_K_MAJOR 1   /* B^T is given: N x K, row-major */
+
+/* Return codes */
+#define GEMM_OK 0
+#define GEMM_ERR_INVALID_VALUE 1      /* negative size, ld too small, bad layout, NULL with a nonzero extent, C overlaps A or B, size beyond the limits */
+#define GEMM_ERR_MISALIGNED 2         /* a pointer not aligned to its element size */
+#define GEMM_ERR_UNSUPPORTED_DEVICE 3 /* the current device is not compute capability 10.3 (sm_103) */
+#define GEMM_ERR_LAUNCH 4             /* the CUDA runtime refused the launch (see cudaGetLastError) */
+#define GEMM_ERR_NOT_DEVICE_MEMORY 5  /* a pointer is not device or managed memory of the current device */
+#define GEMM_ERR_DRIVER 6             /* the driver's tensor-map encoder is missing or rejected a map */
+#define GEMM_ERR_DEVICE_TIMEOUT 7     /* returned by gemm_get_device_status when a kernel gave up waiting */
+
+/* Limits: M, N, K < 2^31; the number of 128 x 256 output tiles < 2^31. */
+
+/* C = A . B with TF32 tensor-core inputs; A, B, C fp32. */
+int gemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
+              int64_t ldc, int layout, void* stream);
+
+/* C = A . B with IEEE binary16 inputs and output (uint16_t bit patterns). */
+int gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+             uint16_t* C, int64_t ldc, int layout, void* stream);
+
+/* C = A . B with bfloat16 inputs and output (uint16_t bit patterns). */
+int gemm_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+              uint16_t* C, int64_t ldc, int layout, void* stream);
+
+/* Static English text for a return code; never NULL. */
+const char* gemm_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads the current device's status word into
+ * *out: 0 when no kernel gave up waiting since the last reset, else a nonzero
+ * code (bits 0-3 kind: 1 = wait time limit exceeded; bits 4-7 role: 1 TMA
+ * producer, 2 MMA issuer, 3 epilogue, 4 copy warps, 5 teardown; bits 8-15
+ * pipeline stage; bits 16-31 CTA index). Returns GEMM_OK, or
+ * GEMM_ERR_DEVICE_TIMEOUT when *out is nonzero, or GEMM_ERR_LAUNCH when the
+ * synchronisation failed. The word is sticky until gemm_reset_device_status.
+ */
+int gemm_get_device_status(void* stream, uint32_t* out);
+
+/* Clears the current device's status word (synchronous). */
+int gemm_reset_device_status(void);
+
+/*
+ * Test hooks, process-wide, for subsequent calls. `wait_limit_ns` bounds every
+ * wait inside the kernels (0 keeps the default of 1 s). Flag bit 0 makes the
+ * TMA producer issue nothing, so the MMA issuer's first wait runs out: the
+ * kernel records a timeout and returns with C unspecified. Pass 0, 0 to restore.
+ */
+int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t gemm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGT_GEMM_H */

@@ -1,0 +1,208 @@
+"""Parity of the CUDA GEMM with the CPU oracle, through the C interface.
+
+Acceptance per output entry (see oracle/check.py): |C_gpu - C_ref| <=
+1e-3 * S + one output ulp for FP16/BF16 inputs and <= 4e-3 * S for TF32,
+S = sum_k |A[i][k]| |B[k][j]|. Small shapes and every workload up to 4096 are
+checked in full; the larger workloads on >= 4096 seeded sampled entries plus
+corners and the last row and column.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_gemm_tensor_gb300 import gemm, inputs
+
+pytestmark = pytest.mark.gpu
+
+TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "tf32": torch.float32}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_gemm_tensor_gb300 import build
+    build.build()
+    gemm.load()
+    gemm.set_debug(0, 0)
+    gemm.reset_device_status()
+    yield
+    assert gemm.device_status() == 0
+
+
+def _views(p, A, B):
+    a = A[:, :p.K]
+    b = B[:, :p.N] if p.layout == 0 else B[:, :p.K]
+    return a, b
+
+
+def _run(p, ldc=None, out_rows=None, fill=None):
+    """Run the product of problem p on the GPU; returns (C logical view, C buffer)."""
+    A = p.a.cuda()
+    B = p.b.cuda()
+    a, b = _views(p, A, B)
+    ldc = p.N if ldc is None else ldc
+    rows = p.M if out_rows is None else out_rows
+    Cbuf = torch.empty((rows, ldc), dtype=TORCH_DT[p.dtype], device="cuda")
+    if fill is not None:
+        Cbuf.fill_(fill)
+    C = Cbuf[:p.M, :p.N]
+    gemm.matmul(a, b, C, layout=p.layout)
+    torch.cuda.synchronize()
+    return C, Cbuf
+
+
+def _check_full(p, C):
+    c_ref = oracle.gemm(p.M, p.N, p.K, p.a, p.lda, p.b, p.ldb, p.layout)
+    s = oracle.abs_gemm(p.M, p.N, p.K, p.a, p.lda, p.b, p.ldb, p.layout)
+    res = oracle.check(C.cpu().double().numpy(), c_ref, s, p.dtype)
+    assert res["ok"], res
+    return res
+
+
+def _check_sampled(p, C, seed, count=4096):
+    r, c = inputs.sample_entries(p.M, p.N, count, seed)
+    got = C[torch.from_numpy(r).cuda(), torch.from_numpy(c).cuda()].cpu().double().numpy()
+    c_ref, s = oracle.gemm_entries(p.M, p.N, p.K, p.a, p.lda, p.b, p.ldb, p.layout, r, c)
+    res = oracle.check(got, c_ref, s, p.dtype)
+    assert res["ok"], res
+    return res
+
+
+SMALL_SHAPES = [(1, 1, 1), (7, 13, 5), (128, 256, 64), (129, 257, 65), (300, 520, 200), (257, 300, 1000),
+                (64, 600, 8), (1000, 40, 333)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("shape", SMALL_SHAPES)
+def test_small_shapes_full(dtype, layout, shape):
+    M, N, K = shape
+    # 8-element-padded pitches keep every operand on the TMA path
+    pad = 8 if dtype != "tf32" else 4
+    lda = -(-K // pad) * pad
+    ldb = -(-(N if layout == 0 else K) // pad) * pad
+    p = inputs.make_problem("small", dtype, M, N, K, seed_a=M * 7 + K, seed_b=N * 5 + K, layout=layout,
+                            lda=lda, ldb=ldb, dist_a="normal")
+    C, _ = _run(p)
+    _check_full(p, C)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_small_integers_bit_exact(dtype, layout):
+    """Integer operands in [-4, 4]: every product and partial sum is exact in
+    fp32, so C must equal the oracle rounded once (RNE) to the output type."""
+    M, N, K = 300, 520, 700
+    rng = np.random.default_rng(17 + layout)
+    Ai = torch.from_numpy(rng.integers(-4, 5, size=(M, K)).astype(np.float32)).to(TORCH_DT[dtype])
+    Bi = torch.from_numpy(rng.integers(-4, 5, size=(K, N)).astype(np.float32)).to(TORCH_DT[dtype])
+    Bs = Bi if layout == 0 else Bi.T.contiguous()
+    p = inputs.Problem("int", dtype, M, N, K, Ai, K, Bs, (N if layout == 0 else K), layout, N)
+    C, _ = _run(p)
+    c_ref = oracle.gemm(M, N, K, p.a, p.lda, p.b, p.ldb, layout)
+    want = torch.from_numpy(c_ref).to(TORCH_DT[dtype])
+    assert torch.equal(C.cpu(), want)
+
+
+@pytest.mark.parametrize("dtype,lda,ldb,ldc", [
+    ("bf16", 301, 523, 521),   # odd pitches: 2-byte copy granularity, unaligned C
+    ("bf16", 302, 522, 522),   # 4-byte granularity
+    ("f16", 204, 524, 526),    # 8-byte granularity for A, 4 for B
+    ("tf32", 201, 521, 523),   # 4-byte granularity
+    ("tf32", 202, 522, 520),   # 8-byte granularity, aligned C
+])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_unaligned_pitches_full(dtype, lda, ldb, ldc, layout):
+    """Row pitches TMA cannot address go through the copy warps."""
+    M, N, K = 300, 520, 200
+    if layout == 1:
+        ldb = lda + 3
+    p = inputs.make_problem("unal", dtype, M, N, K, lda=lda, ldb=ldb, layout=layout, seed_a=5, seed_b=6)
+    C, Cbuf = _run(p, ldc=ldc, fill=7.0)
+    _check_full(p, C)
+    assert torch.all(Cbuf[:, N:] == 7.0)
+
+
+def test_output_guard_band_untouched():
+    """C inside a larger buffer (ldc > N, extra rows): the padding keeps its sentinel."""
+    p = inputs.make_problem("guard", "bf16", 200, 300, 128, seed_a=1, seed_b=2)
+    C, Cbuf = _run(p, ldc=320, out_rows=210, fill=-3.0)
+    _check_full(p, C)
+    assert torch.all(Cbuf[:, 300:] == -3.0)
+    assert torch.all(Cbuf[200:, :] == -3.0)
+
+
+def test_k_zero_writes_zeros_and_empty_is_no_op():
+    for dt in ("bf16", "tf32"):
+        C = torch.full((33, 70), 5.0, dtype=TORCH_DT[dt], device="cuda")
+        A = torch.empty((33, 0), dtype=TORCH_DT[dt], device="cuda")
+        B = torch.empty((0, 70), dtype=TORCH_DT[dt], device="cuda")
+        gemm.matmul(A, B, C)
+        torch.cuda.synchronize()
+        assert torch.all(C == 0)
+    C = torch.full((0, 5), 5.0, dtype=torch.bfloat16, device="cuda")
+    gemm.matmul(torch.empty((0, 8), dtype=torch.bfloat16, device="cuda"),
+                torch.empty((8, 5), dtype=torch.bfloat16, device="cuda"), C)
+
+
+def test_deterministic_bitwise():
+    p = inputs.make_problem("det", "bf16", 1000, 1500, 2000, seed_a=3, seed_b=4)
+    C1, _ = _run(p)
+    C2, _ = _run(p)
+    assert torch.equal(C1, C2)
+
+
+def test_rejects_host_memory_and_overlap():
+    A = torch.ones((64, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.ones((64, 64), dtype=torch.bfloat16, device="cuda")
+    H = torch.ones((64, 64), dtype=torch.bfloat16)
+    C = torch.empty((64, 64), dtype=torch.bfloat16, device="cuda")
+    code = gemm.gemm_bf16(64, 64, 64, H.data_ptr(), 64, B.data_ptr(), 64, C.data_ptr(), 64, 0, None)
+    assert code == gemm.GEMM_ERR_NOT_DEVICE_MEMORY
+    code = gemm.gemm_bf16(64, 64, 64, A.data_ptr(), 64, B.data_ptr(), 64, A.data_ptr(), 64, 0, None)
+    assert code == gemm.GEMM_ERR_INVALID_VALUE
+
+
+def test_wait_time_limit_reports_and_recovers():
+    """A producer that issues nothing leaves the MMA issuer's first wait
+    unsatisfied: the kernel gives up after the (short) limit, records a
+    timeout, and the next normal launch is correct."""
+    p = inputs.make_problem("to", "bf16", 256, 512, 256, seed_a=8, seed_b=9)
+    A, B = p.a.cuda(), p.b.cuda()
+    C = torch.empty((256, 512), dtype=torch.bfloat16, device="cuda")
+    gemm.reset_device_status()
+    gemm.set_debug(1, 20_000_000)  # 20 ms
+    try:
+        gemm.matmul(A, B, C)
+        word = gemm.device_status()
+    finally:
+        gemm.set_debug(0, 0)
+    assert word & 0xF == 1
+    # the MMA issuer (2) or the epilogue (3) runs out first; both wait on the stalled pipeline
+    assert (word >> 4) & 0xF in (2, 3)
+    gemm.reset_device_status()
+    C, _ = _run(p)
+    _check_full(p, C)
+    assert gemm.device_status() == 0
+
+
+# ---------------------------------------------------------------- the workloads
+@pytest.mark.parametrize("name", ["bf16_512", "bf16_1024", "bf16_2048", "tf32_4096", "f16_4096", "bf16_4096",
+                                  "bf16_ragged"])
+def test_workload_full(name):
+    p = inputs.workload(name)
+    C, _ = _run(p)
+    res = _check_full(p, C)
+    print(name, res)
+
+
+@pytest.mark.parametrize("name", ["bf16_8192", "bf16_16384", "bf16_proj"])
+def test_workload_sampled(name):
+    p = inputs.workload(name)
+    n = inputs.WORKLOADS[name]["n"]
+    C, _ = _run(p)
+    res = _check_sampled(p, C, 3000 + n)
+    print(name, res)
