@@ -32,6 +32,16 @@
 
 #include "ptx.cuh"
 
+// Geometry of the 32-byte-atom swizzle (MN-major 32-bit operands): stride
+// between K-row groups in the descriptor, and which row bits select the
+// XOR pattern of the 32-byte chunks.
+#ifndef DGT_ATOM32_SBO
+#define DGT_ATOM32_SBO 512
+#endif
+#ifndef DGT_ATOM32_ROWSHIFT
+#define DGT_ATOM32_ROWSHIFT 0
+#endif
+
 namespace dgt {
 
 enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_TF32 = 2 };
@@ -99,6 +109,11 @@ struct Cfg {
   static constexpr int BOXN = 128 / ES;     // MN-major B: N elements per 128-byte box row
   static constexpr int NBOX = BN / BOXN;    // MN-major B: boxes per stage
   static constexpr int BOX_BYTES = BK * 128;
+  // MN-major B of 32-bit elements uses the 128-byte swizzle with 32-byte
+  // atoms (16-bit MN-major and every K-major tile use 16-byte atoms).
+  static constexpr bool B_ATOM32 = (ES == 4) && !B_KMAJOR;
+  static constexpr uint32_t B_SWZ = B_ATOM32 ? SWZ_128B_ATOM32 : SWZ_128B;
+  static constexpr uint32_t B_SBO = B_ATOM32 ? DGT_ATOM32_SBO : 1024;
   static constexpr int ACC_COLS = BN;       // fp32 accumulator columns of one buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
@@ -209,8 +224,19 @@ __device__ __forceinline__ void copy_kmajor_tile(uint32_t sdst, const uint8_t* b
   }
 }
 
+// Byte position of `byte` (0..127) of row `k` inside a 128-byte-swizzled
+// tile: 16-byte chunks XOR (k mod 8), or 32-byte chunks XOR the row bits the
+// 32-byte-atom mode uses.
+template <bool ATOM32>
+__device__ __forceinline__ uint32_t swz_pos(int k, int byte) {
+  if constexpr (ATOM32)
+    return (((byte >> 5) ^ ((k >> DGT_ATOM32_ROWSHIFT) & 3)) << 5) | (byte & 31);
+  else
+    return (((byte >> 4) ^ (k & 7)) << 4) | (byte & 15);
+}
+
 // One MN-major B tile: NBOX boxes, each BK rows (K) of 128 bytes along N.
-template <int ES, int BK, int NBOX, int BOX_BYTES>
+template <int ES, int BK, int NBOX, int BOX_BYTES, bool ATOM32>
 __device__ __forceinline__ void copy_mnmajor_tile(uint32_t sdst, const uint8_t* base, long long ld_bytes, int n0,
                                                   int N, int k0, int K, int gran, int tid) {
   const int per_row = 128 / gran;
@@ -221,7 +247,7 @@ __device__ __forceinline__ void copy_mnmajor_tile(uint32_t sdst, const uint8_t* 
     const int byte = (c - row * per_row) * gran;
     const int box = row / BK;
     const int k = row - box * BK;
-    const uint32_t dst = sdst + box * BOX_BYTES + k * 128 + ((((byte >> 4) ^ (k & 7)) << 4) | (byte & 15));
+    const uint32_t dst = sdst + box * BOX_BYTES + k * 128 + swz_pos<ATOM32>(k, byte);
     const int gk = k0 + k;
     const long long gn = static_cast<long long>(n0) * ES + box * 128 + byte;
     int valid = 0;
@@ -400,12 +426,12 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t b_addr = sB + s * Cf::B_BYTES;
 #pragma unroll
           for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
-            const uint64_t ad = sdesc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t ad = sdesc(a_addr + kk * 32, 16, 1024, SWZ_128B);
             uint64_t bd;
             if constexpr (B_KMAJOR)
-              bd = sdesc_sw128(b_addr + kk * 32, 16, 1024);
+              bd = sdesc(b_addr + kk * 32, 16, 1024, SWZ_128B);
             else
-              bd = sdesc_sw128(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, 1024);
+              bd = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
             const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
             if constexpr (KIND == KIND_TF32)
               mma_tf32(d, ad, bd, Cf::IDESC, acc);
@@ -474,7 +500,7 @@ __global__ void __launch_bounds__(320, 1)
             copy_kmajor_tile<Cf::ES>(sB + s * Cf::B_BYTES, Bb, ldb_b, Cf::BN, nb * Cf::BN, p.N, kb * Cf::BK, p.K,
                                      p.copy_bytes, ctid);
           else
-            copy_mnmajor_tile<Cf::ES, Cf::BK, Cf::NBOX, Cf::BOX_BYTES>(sB + s * Cf::B_BYTES, Bb, ldb_b,
+            copy_mnmajor_tile<Cf::ES, Cf::BK, Cf::NBOX, Cf::BOX_BYTES, Cf::B_ATOM32>(sB + s * Cf::B_BYTES, Bb, ldb_b,
                                                                         nb * Cf::BN, p.N, kb * Cf::BK, p.K,
                                                                         p.copy_bytes, ctid);
         }

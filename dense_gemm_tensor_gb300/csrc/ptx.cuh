@@ -129,19 +129,23 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- descriptors
-// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle:
+// Shared-memory matrix descriptor for tcgen05.mma:
 //   bits  0-13  start address >> 4
 //   bits 16-29  leading-dimension byte offset >> 4
 //   bits 32-45  stride-dimension byte offset >> 4
 //   bits 46-48  fixed 0b001
 //   bits 49-51  base offset (0: every operand tile starts 1024-byte aligned)
-//   bits 61-63  swizzle mode (2 = 128-byte swizzle)
+//   bits 61-63  swizzle mode: 2 = 128-byte swizzle of 16-byte chunks,
+//               1 = 128-byte swizzle of 32-byte chunks
 // K-major operand: rows of 128 bytes along K, 8-row groups `sbo` apart (lbo unused).
-// MN-major operand: 128-byte rows along M/N, 8-row K groups `sbo` apart, and
-// consecutive 128-byte-wide M/N slabs `lbo` apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// MN-major operand: 128-byte rows along M/N, K-row groups (one swizzle atom
+// high) `sbo` apart, and consecutive 128-byte-wide M/N slabs `lbo` apart.
+enum : uint32_t { SWZ_128B = 2, SWZ_128B_ATOM32 = 1 };
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+         (static_cast<uint64_t>(swizzle) << 61);
 }
 
 }  // namespace dgt
