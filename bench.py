@@ -85,7 +85,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         return self
@@ -194,8 +194,9 @@ def run_ours(args, world, rank, local):
         ms = statistics.mean(e[dt][0].elapsed_time(e[dt][1]) for e in evs)
         ach = FLOP_PER_PRODUCT / (ms * 1e-3) / 1e12
         pk = peak_for(dt, peaks)
+        pk_sus = peaks.get("bf16_tflops_sustained", pk) * NOMINAL_RATIO[dt]
         per_dtype[dt] = {"kernel_ms": round(ms, 5), "tflops": round(ach, 2), "peak_tflops": round(pk, 1),
-                         "frac": round(ach / pk, 4)}
+                         "frac": round(ach / pk, 4), "frac_of_sustained_peak": round(ach / pk_sus, 4)}
     dominant = max(DTYPES, key=lambda d: per_dtype[d]["kernel_ms"])
     total_flop = FLOP_PER_PRODUCT * len(DTYPES) * args.steps * world
     value = total_flop / (elapsed_ms * 1e-3) / 1e12
@@ -330,8 +331,8 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

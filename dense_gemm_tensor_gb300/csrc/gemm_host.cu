@@ -35,6 +35,9 @@ std::atomic<uint32_t> g_epoch{1};
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint32_t> g_debug_flags{0};
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_force_variant{0};
+std::atomic<int> g_force_bn{0};
+std::atomic<int> g_force_raster{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -128,6 +131,97 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Co-resident CTA pairs of each pair-kernel variant, per device (-1 = not queried yet).
+std::atomic<int> g_pair_clusters[kMaxDevices][3][2][2];
+std::once_flag g_pair_once;
+
+int pair_clusters(int dev, int kind, bool kmajor, int bn) {
+  std::call_once(g_pair_once, [] {
+    for (auto& a : g_pair_clusters)
+      for (auto& b : a)
+        for (auto& c : b)
+          for (auto& d : c) d.store(-1);
+  });
+  std::atomic<int>& slot = g_pair_clusters[dev][kind][kmajor ? 1 : 0][bn == 256 ? 0 : 1];
+  int n = slot.load(std::memory_order_acquire);
+  if (n < 0) {
+    n = kind == KIND_TF32 ? pair_clusters_tf32(kmajor, bn)
+        : kind == KIND_BF16 ? pair_clusters_bf16(kmajor, bn)
+                            : pair_clusters_f16(kmajor, bn);
+    slot.store(n, std::memory_order_release);
+  }
+  return n;
+}
+
+struct TilePlan {
+  bool pair;
+  int bn;
+  int raster;
+  int grid;  // CTAs
+};
+
+// Picks the kernel (single CTA or CTA pair), the tile width and the tile order.
+//
+// Cost model, per SM and per 128-byte k-slab of a tile: the MMA needs 2 * (tile
+// columns per SM-row block) cycles (128 x BN x one slab at the dense rate), and
+// the SM must receive 16 KB of A plus (B columns it loads) x 128 bytes, at
+// about 68 bytes per cycle (measured on GB300 for this kernel); the slower of
+// the two sets the slab time. A CTA pair computes a 256 x BN tile from half the
+// B bytes per SM. The grid holds one CTA per SM, so a product of T tiles takes
+// ceil(T / concurrent tiles) rounds; the plan with the least total time wins.
+// The band height keeps a band's A rows and the B tiles in flight inside L2.
+TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es, bool kmajor, bool all_tma,
+                     int sms) {
+  const int atom = 128 / es;  // MN-major B is fetched in whole 128-byte slabs
+  const int64_t kslabs = (K * es + 127) / 128;
+  const int fv = g_force_variant.load(std::memory_order_relaxed);
+  const int fb = g_force_bn.load(std::memory_order_relaxed);
+  const int fr = g_force_raster.load(std::memory_order_relaxed);
+  TilePlan best{false, 256, 8, sms};
+  double best_cost = -1.0;
+  auto consider = [&](bool pair, int bn) {
+    if (fv == 1 && pair) return;
+    if (fv == 2 && !pair) return;
+    if (fb && fb != bn) return;
+    int cols;  // B columns one SM loads per slab
+    if (pair) {
+      if (!all_tma) return;
+      if (!kmajor && (bn / 2) % atom != 0) return;
+      cols = bn / 2;
+    } else {
+      cols = kmajor ? bn : (bn + atom - 1) / atom * atom;
+    }
+    int conc;  // tiles in flight
+    if (pair) {
+      conc = pair_clusters(dev, kind, kmajor, bn);
+      if (conc <= 0) return;
+    } else {
+      conc = sms;
+    }
+    const int64_t rows = pair ? 256 : 128;
+    const int64_t tiles = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + conc - 1) / conc;
+    const double mma = 2.0 * bn;
+    const double bytes = 128.0 * 128.0 + 128.0 * cols;
+    const double slab = mma > bytes / 68.0 ? mma : bytes / 68.0;
+    const double cost = double(waves) * (double(kslabs) * slab + 600.0);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      const int64_t tiles_m = (M + rows - 1) / rows;
+      const int64_t grid_tiles = tiles < conc ? tiles : conc;
+      best = TilePlan{pair, bn, int(tiles_m < 8 ? tiles_m : 8), int(pair ? 2 * grid_tiles : grid_tiles)};
+    }
+  };
+  for (int bn : kPairTileWidths) consider(true, bn);
+  for (int bn : kTileWidths) consider(false, bn);
+  if (best_cost < 0) {  // a forced combination that does not apply: fall back to the single-CTA default
+    const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
+    best = TilePlan{false, 256, 8, int(tiles < sms ? tiles : sms)};
+  }
+  if (fr) best.raster = fr;
+  return best;
+}
+
 int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
              void* C, int64_t ldc, int layout, void* stream_ptr) {
   const int es = (kind == KIND_TF32) ? 4 : 2;
@@ -142,8 +236,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     if (lda > (int64_t(1) << 40) / es || ldb > (int64_t(1) << 40) / es) return GEMM_ERR_INVALID_VALUE;
   }
   if (ldc > (int64_t(1) << 40) / es) return GEMM_ERR_INVALID_VALUE;
-  const int64_t tiles_m = (M + 127) / 128, tiles_n = (N + 255) / 256;
-  if (tiles_m * tiles_n > kLim) return GEMM_ERR_INVALID_VALUE;
+  if (((M + 127) / 128) * ((N + 127) / 128) > kLim) return GEMM_ERR_INVALID_VALUE;
 
   auto mis = [es](const void* p) { return (reinterpret_cast<uintptr_t>(p) % es) != 0; };
   if (mis(C) || (K > 0 && (mis(A) || mis(B)))) return GEMM_ERR_MISALIGNED;
@@ -176,6 +269,14 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   LaunchPlan L;
   memset(&L, 0, sizeof(L));
   GemmParams& p = L.p;
+  const int ga = granularity(A, lda, es), gb = granularity(B, ldb, es);
+  const bool kmajor = layout == GEMM_B_K_MAJOR;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  const TilePlan plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, ga == 16 && gb == 16, dev->sm_count);
+  const int bn = plan.bn;
+  const int64_t tiles_m = (M + (plan.pair ? 255 : 127)) / (plan.pair ? 256 : 128);
+  const int64_t tiles_n = (N + bn - 1) / bn;
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
@@ -183,14 +284,13 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   p.tiles_n = int(tiles_n);
   p.num_tiles = int(tiles_m * tiles_n);
   p.num_kb = int((K * es + 127) / 128);
-  p.raster = 8;
+  p.raster = plan.raster;
   p.A = A;
   p.lda = lda;
   p.B = B;
   p.ldb = ldb;
   p.C = C;
   p.ldc = ldc;
-  const int ga = granularity(A, lda, es), gb = granularity(B, ldb, es);
   p.a_tma = ga == 16;
   p.b_tma = gb == 16;
   p.copy_bytes = 16;
@@ -213,14 +313,17 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   if (p.b_tma) {
     bool ok;
     if (layout == GEMM_B_K_MAJOR)
-      ok = encode_2d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, bk, 256);
+      ok = encode_2d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, bk,
+                     uint32_t(plan.pair ? bn / 2 : bn));
     else
       ok = encode_2d(&L.tmB, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, 128 / es, bk,
                      es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return GEMM_ERR_DRIVER;
   }
-  L.b_kmajor = layout == GEMM_B_K_MAJOR;
-  L.grid = p.num_tiles < dev->sm_count ? p.num_tiles : dev->sm_count;
+  L.b_kmajor = kmajor;
+  L.pair = plan.pair;
+  L.bn = bn;
+  L.grid = plan.grid;
   L.threads = (p.a_tma && p.b_tma) ? 192 : 320;
   L.stream = stream;
 
@@ -304,5 +407,21 @@ int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns) {
 }
 
 uint64_t gemm_launch_count(void) { return dgt::g_launches.load(); }
+
+int gemm_set_tuning(int variant, int tile_n, int raster) {
+  if (variant < 0 || variant > 2 || raster < 0) return GEMM_ERR_INVALID_VALUE;
+  if (tile_n != 0) {
+    bool ok = false;
+    if (variant != 2)
+      for (int w : dgt::kTileWidths) ok = ok || (w == tile_n);
+    if (variant != 1)
+      for (int w : dgt::kPairTileWidths) ok = ok || (w == tile_n);
+    if (!ok) return GEMM_ERR_INVALID_VALUE;
+  }
+  dgt::g_force_variant.store(variant);
+  dgt::g_force_bn.store(tile_n);
+  dgt::g_force_raster.store(raster);
+  return GEMM_OK;
+}
 
 }  // extern "C"

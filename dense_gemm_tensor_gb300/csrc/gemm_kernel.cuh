@@ -94,34 +94,39 @@ struct GemmParams {
   unsigned long long wait_limit_ns;
 };
 
-template <int KIND, bool B_KMAJOR>
+template <int KIND, bool B_KMAJOR, int BN_>
 struct Cfg {
   using T = typename KindTraits<KIND>::T;
   static constexpr int ES = sizeof(T);
   static constexpr int BM = 128;
-  static constexpr int BN = 256;
+  static constexpr int BN = BN_;            // output tile width (multiple of 32, <= 256)
   static constexpr int BK = 128 / ES;       // one 128-byte swizzle row of K per stage
   static constexpr int UK = 32 / ES;        // K of one tcgen05.mma (16 for 16-bit, 8 for tf32)
   static constexpr int KSTEPS = BK / UK;    // MMAs per stage
-  static constexpr int STAGES = 4;
   static constexpr int A_BYTES = BM * 128;  // 16 KB
-  static constexpr int B_BYTES = BN * 128;  // 32 KB
   static constexpr int BOXN = 128 / ES;     // MN-major B: N elements per 128-byte box row
-  static constexpr int NBOX = BN / BOXN;    // MN-major B: boxes per stage
+  static constexpr int NBOX = (BN + BOXN - 1) / BOXN;  // MN-major B: boxes per stage (last may be partly used)
   static constexpr int BOX_BYTES = BK * 128;
+  static constexpr int B_BYTES = B_KMAJOR ? BN * 128 : NBOX * BOX_BYTES;
   // MN-major B of 32-bit elements uses the 128-byte swizzle with 32-byte
   // atoms (16-bit MN-major and every K-major tile use 16-byte atoms).
   static constexpr bool B_ATOM32 = (ES == 4) && !B_KMAJOR;
   static constexpr uint32_t B_SWZ = B_ATOM32 ? SWZ_128B_ATOM32 : SWZ_128B;
   static constexpr uint32_t B_SBO = B_ATOM32 ? DGT_ATOM32_SBO : 1024;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM_LIMIT = 232448;  // opt-in dynamic shared memory per block
+  static constexpr int RESERVED = 1024 /*align slack*/ + 256 /*barriers*/;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int ACC_COLS = BN;       // fp32 accumulator columns of one buffer
-  static constexpr int TMEM_COLS = 2 * ACC_COLS;
+  static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // power of two >= 2 * BN
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-  static constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
-  static constexpr int THREADS_TMA = 192;   // 4 epilogue + producer + MMA warps
-  static constexpr int THREADS_COPY = 320;  // + 4 copy warps
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + RESERVED;
   static constexpr int COPY_LAG = 2;        // stages a copy warp keeps in flight before signalling
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+  static_assert(STAGES >= 3, "pipeline depth");
   static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
 
   // Instruction descriptor: D fp32, A/B format, A K-major, B K- or MN-major, N, M.
   static constexpr uint32_t IDESC = (1u << 4) | (KindTraits<KIND>::fmt << 7) | (KindTraits<KIND>::fmt << 10) |
@@ -317,11 +322,11 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, in
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int KIND, bool B_KMAJOR>
+template <int KIND, bool B_KMAJOR, int BN>
 __global__ void __launch_bounds__(320, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
-  using Cf = Cfg<KIND, B_KMAJOR>;
+  using Cf = Cfg<KIND, B_KMAJOR, BN>;
   constexpr int S = Cf::STAGES;
 
   extern __shared__ uint8_t smem_raw[];
@@ -462,7 +467,7 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
       const int ncols = min(Cf::BN, p.N - nb * Cf::BN);
 #pragma unroll 1
-      for (int c = 0; c < Cf::BN / 32; ++c) {
+      for (int c = 0; c < BN / 32; ++c) {
         if (c * 32 >= ncols) break;  // warp-uniform
         uint32_t r[32];
         __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane stores

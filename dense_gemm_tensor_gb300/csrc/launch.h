@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_pair.cuh"
 
 namespace dgt {
 
@@ -13,6 +14,8 @@ struct LaunchPlan {
   CUtensorMap tmB;  // valid when p.b_tma
   GemmParams p;
   bool b_kmajor;
+  bool pair;  // CTA-pair kernel (cluster of 2, cta_group::2)
+  int bn;     // output tile width: one of kTileWidths (single) or kPairTileWidths (pair)
   int grid;
   int threads;
   cudaStream_t stream;
@@ -21,35 +24,123 @@ struct LaunchPlan {
 cudaError_t launch_f16(const LaunchPlan& L);
 cudaError_t launch_bf16(const LaunchPlan& L);
 cudaError_t launch_tf32(const LaunchPlan& L);
+int pair_clusters_f16(bool kmajor, int bn);
+int pair_clusters_bf16(bool kmajor, int bn);
+int pair_clusters_tf32(bool kmajor, int bn);
 cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count);
 
+// Tile widths the kernels are built for (the host picks one per call).
+constexpr int kTileWidths[] = {256, 224, 192, 128};
+constexpr int kPairTileWidths[] = {256, 128};
+
+
 // Sets the kernel's dynamic shared-memory limit once per device, then launches.
-template <int KIND>
-cudaError_t launch_kind(const LaunchPlan& L) {
-  static int configured[2][64] = {};
+template <int KIND, bool KMAJ, int BN>
+cudaError_t launch_variant(const LaunchPlan& L) {
+  static int configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (L.b_kmajor) {
-    auto kern = gemm_kernel<KIND, true>;
-    constexpr int smem = Cfg<KIND, true>::SMEM_BYTES;
-    if (dev < 64 && !__atomic_load_n(&configured[1][dev], __ATOMIC_ACQUIRE)) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      __atomic_store_n(&configured[1][dev], 1, __ATOMIC_RELEASE);
-    }
-    kern<<<L.grid, L.threads, smem, L.stream>>>(L.tmA, L.tmB, L.p);
-  } else {
-    auto kern = gemm_kernel<KIND, false>;
-    constexpr int smem = Cfg<KIND, false>::SMEM_BYTES;
-    if (dev < 64 && !__atomic_load_n(&configured[0][dev], __ATOMIC_ACQUIRE)) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      __atomic_store_n(&configured[0][dev], 1, __ATOMIC_RELEASE);
-    }
-    kern<<<L.grid, L.threads, smem, L.stream>>>(L.tmA, L.tmB, L.p);
+  auto kern = gemm_kernel<KIND, KMAJ, BN>;
+  constexpr int smem = Cfg<KIND, KMAJ, BN>::SMEM_BYTES;
+  if (dev >= 64 || !__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
   }
+  kern<<<L.grid, L.threads, smem, L.stream>>>(L.tmA, L.tmB, L.p);
   return cudaGetLastError();
+}
+
+template <int KIND, bool KMAJ>
+cudaError_t launch_layout(const LaunchPlan& L) {
+  switch (L.bn) {
+    case 256: return launch_variant<KIND, KMAJ, 256>(L);
+    case 224: return launch_variant<KIND, KMAJ, 224>(L);
+    case 192: return launch_variant<KIND, KMAJ, 192>(L);
+    case 128: return launch_variant<KIND, KMAJ, 128>(L);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+
+template <int KIND, bool KMAJ, int BN>
+cudaError_t launch_pair_variant(const LaunchPlan& L) {
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  auto kern = gemm_kernel_pair<KIND, KMAJ, BN>;
+  constexpr int smem = PairCfg<KIND, KMAJ, BN>::SMEM_BYTES;
+  if (dev >= 64 || !__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(L.grid, 1, 1);
+  cfg.blockDim = dim3(L.threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Co-resident clusters of one pair variant (occupancy query with its launch shape).
+template <int KIND, bool KMAJ, int BN>
+int pair_clusters_variant() {
+  auto kern = gemm_kernel_pair<KIND, KMAJ, BN>;
+  constexpr int smem = PairCfg<KIND, KMAJ, BN>::SMEM_BYTES;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int KIND, bool KMAJ>
+cudaError_t launch_pair_layout(const LaunchPlan& L) {
+  switch (L.bn) {
+    case 256: return launch_pair_variant<KIND, KMAJ, 256>(L);
+    case 128: return launch_pair_variant<KIND, KMAJ, 128>(L);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int KIND>
+int pair_clusters_kind(bool kmajor, int bn) {
+  if (kmajor) return bn == 256 ? pair_clusters_variant<KIND, true, 256>() : pair_clusters_variant<KIND, true, 128>();
+  return bn == 256 ? pair_clusters_variant<KIND, false, 256>() : pair_clusters_variant<KIND, false, 128>();
+}
+
+template <int KIND>
+cudaError_t launch_kind(const LaunchPlan& L) {
+  if (L.pair) return L.b_kmajor ? launch_pair_layout<KIND, true>(L) : launch_pair_layout<KIND, false>(L);
+  return L.b_kmajor ? launch_layout<KIND, true>(L) : launch_layout<KIND, false>(L);
 }
 
 }  // namespace dgt

@@ -71,7 +71,7 @@ extern "C" {
 #define GEMM_ERR_DRIVER 6             /* the driver's tensor-map encoder is missing or rejected a map */
 #define GEMM_ERR_DEVICE_TIMEOUT 7     /* returned by gemm_get_device_status when a kernel gave up waiting */
 
-/* Limits: M, N, K < 2^31; the number of 128 x 256 output tiles < 2^31. */
+/* Limits: M, N, K < 2^31; the number of 128 x 128 output tiles < 2^31. */
 
 /* C = A . B with TF32 tensor-core inputs; A, B, C fp32. */
 int gemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
@@ -112,6 +112,18 @@ int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t gemm_launch_count(void);
+
+/*
+ * Tuning hook, process-wide, for subsequent calls. `variant`: 0 = chosen per
+ * call, 1 = single-CTA kernel (128-row tiles), 2 = CTA-pair kernel (256-row
+ * tiles; only when A and B rows are 16-byte aligned, else the single-CTA
+ * kernel runs). `tile_n`: output tile width, 256, 224, 192 or 128 for the
+ * single-CTA kernel and 256 or 128 for the pair (0 = chosen per call).
+ * `raster`: band height of the tile order in tile rows (0 = chosen per call).
+ * Results do not depend on any of them. Returns GEMM_ERR_INVALID_VALUE for
+ * values outside these sets.
+ */
+int gemm_set_tuning(int variant, int tile_n, int raster);
 
 #ifdef __cplusplus
 }

@@ -92,6 +92,49 @@ def test_small_shapes_full(dtype, layout, shape):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
 @pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("tile_n", [256, 224, 192, 128])
+def test_every_tile_width_full(dtype, layout, tile_n):
+    """Each built tile width, forced, on a ragged multi-tile shape (TMA path)
+    and on an odd-pitch shape (copy-warp path)."""
+    gemm.set_tuning(1, tile_n, 3)
+    try:
+        for (M, N, K, lda, ldb) in [(300, 700, 520, 520, None), (260, 450, 300, 301, 451)]:
+            if ldb is None:
+                ldb = N if layout == 0 else K
+            elif layout == 1:
+                ldb = K + 1
+            p = inputs.make_problem("tw", dtype, M, N, K, lda=lda, ldb=ldb, layout=layout,
+                                    seed_a=tile_n + M, seed_b=tile_n + N)
+            C, _ = _run(p)
+            _check_full(p, C)
+    finally:
+        gemm.set_tuning(0, 0, 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("tile_n", [256, 128])
+def test_pair_kernel_full(dtype, layout, tile_n):
+    """The CTA-pair kernel (256-row tiles over two SMs), forced, on shapes
+    with a ragged pair-row (M = 129: the second CTA's rows are all past M),
+    ragged columns and several waves of tiles."""
+    gemm.set_tuning(2, tile_n, 2)
+    try:
+        for (M, N, K) in [(300, 700, 520), (129, 300, 200), (1000, 1500, 336), (2048, 1024, 64)]:
+            ldb = N if layout == 0 else K
+            pad = 8 if dtype != "tf32" else 4
+            ldb = -(-ldb // pad) * pad
+            p = inputs.make_problem("pair", dtype, M, N, K, lda=-(-K // pad) * pad, ldb=ldb, layout=layout,
+                                    seed_a=tile_n + M + 1, seed_b=tile_n + N + 2, dist_a="normal")
+            C, Cbuf = _run(p, ldc=N + 8, fill=3.0)
+            _check_full(p, C)
+            assert torch.all(Cbuf[:, N:] == 3.0)
+    finally:
+        gemm.set_tuning(0, 0, 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
+@pytest.mark.parametrize("layout", [0, 1])
 def test_small_integers_bit_exact(dtype, layout):
     """Integer operands in [-4, 4]: every product and partial sum is exact in
     fp32, so C must equal the oracle rounded once (RNE) to the output type."""
@@ -166,20 +209,23 @@ def test_rejects_host_memory_and_overlap():
     assert code == gemm.GEMM_ERR_INVALID_VALUE
 
 
-def test_wait_time_limit_reports_and_recovers():
+@pytest.mark.parametrize("variant", [1, 2])
+def test_wait_time_limit_reports_and_recovers(variant):
     """A producer that issues nothing leaves the MMA issuer's first wait
     unsatisfied: the kernel gives up after the (short) limit, records a
-    timeout, and the next normal launch is correct."""
-    p = inputs.make_problem("to", "bf16", 256, 512, 256, seed_a=8, seed_b=9)
+    timeout, and the next normal launch is correct (single-CTA and pair)."""
+    p = inputs.make_problem("to", "bf16", 512, 512, 256, seed_a=8, seed_b=9)
     A, B = p.a.cuda(), p.b.cuda()
-    C = torch.empty((256, 512), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
     gemm.reset_device_status()
     gemm.set_debug(1, 20_000_000)  # 20 ms
+    gemm.set_tuning(variant, 0, 0)
     try:
         gemm.matmul(A, B, C)
         word = gemm.device_status()
     finally:
         gemm.set_debug(0, 0)
+        gemm.set_tuning(0, 0, 0)
     assert word & 0xF == 1
     # the MMA issuer (2) or the epilogue (3) runs out first; both wait on the stalled pipeline
     assert (word >> 4) & 0xF in (2, 3)
