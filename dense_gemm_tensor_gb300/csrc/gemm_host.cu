@@ -35,9 +35,12 @@ std::atomic<uint32_t> g_epoch{1};
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint32_t> g_debug_flags{0};
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+// The plan of the calling thread's last successful launch (see gemm_last_plan).
+thread_local int32_t t_last_plan[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 std::atomic<int> g_force_variant{0};
 std::atomic<int> g_force_bn{0};
 std::atomic<int> g_force_raster{0};
+std::atomic<int> g_force_split{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -157,7 +160,9 @@ struct TilePlan {
   bool pair;
   int bn;
   int raster;
-  int grid;  // CTAs
+  int grid;   // CTAs
+  int split;  // pair kernel: column slices per tile of the last partial round (1 or 2)
+  int conc;   // tiles in flight at once (SMs, or co-resident CTA pairs)
 };
 
 // Picks the kernel (single CTA or CTA pair), the tile width and the tile order.
@@ -177,8 +182,13 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
   const int fv = g_force_variant.load(std::memory_order_relaxed);
   const int fb = g_force_bn.load(std::memory_order_relaxed);
   const int fr = g_force_raster.load(std::memory_order_relaxed);
-  TilePlan best{false, 256, 8, sms};
+  TilePlan best{false, 256, 8, sms, 1, sms};
   double best_cost = -1.0;
+  auto slab_cycles = [&](int bn, int cols) {
+    const double mma = 2.0 * bn;
+    const double bytes = 128.0 * 128.0 + 128.0 * cols;
+    return mma > bytes / 66.0 ? mma : bytes / 66.0;
+  };
   auto consider = [&](bool pair, int bn) {
     if (fv == 1 && pair) return;
     if (fv == 2 && !pair) return;
@@ -200,23 +210,29 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
     }
     const int64_t rows = pair ? 256 : 128;
     const int64_t tiles = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
-    const int64_t waves = (tiles + conc - 1) / conc;
-    const double mma = 2.0 * bn;
-    const double bytes = 128.0 * 128.0 + 128.0 * cols;
-    const double slab = mma > bytes / 68.0 ? mma : bytes / 68.0;
-    const double cost = double(waves) * (double(kslabs) * slab + 600.0);
+    const int64_t full = tiles / conc, rest = tiles % conc;
+    // pair kernel: the last partial round may go as half-width slices on twice the pairs
+    const int fs = g_force_split.load(std::memory_order_relaxed);
+    const bool can_split =
+        fs != 1 && pair && rest > 0 && 2 * rest <= conc && (kmajor || (bn / 4) % atom == 0);
+    const int split = can_split ? 2 : 1;
+    const double tile_cost = double(kslabs) * slab_cycles(bn, cols) + 600.0;
+    double cost = double(full) * tile_cost;
+    if (rest > 0) cost += split == 2 ? double(kslabs) * slab_cycles(bn / 2, cols / 2) + 600.0 : tile_cost;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       const int64_t tiles_m = (M + rows - 1) / rows;
-      const int64_t grid_tiles = tiles < conc ? tiles : conc;
-      best = TilePlan{pair, bn, int(tiles_m < 8 ? tiles_m : 8), int(pair ? 2 * grid_tiles : grid_tiles)};
+      const int64_t work = tiles + (split - 1) * rest;
+      const int64_t grid_tiles = work < conc ? work : conc;
+      best = TilePlan{pair, bn, int(tiles_m < 8 ? tiles_m : 8), int(pair ? 2 * grid_tiles : grid_tiles), split,
+                      conc};
     }
   };
   for (int bn : kPairTileWidths) consider(true, bn);
   for (int bn : kTileWidths) consider(false, bn);
   if (best_cost < 0) {  // a forced combination that does not apply: fall back to the single-CTA default
     const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
-    best = TilePlan{false, 256, 8, int(tiles < sms ? tiles : sms)};
+    best = TilePlan{false, 256, 8, int(tiles < sms ? tiles : sms), 1, sms};
   }
   if (fr) best.raster = fr;
   return best;
@@ -283,6 +299,13 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   p.tiles_m = int(tiles_m);
   p.tiles_n = int(tiles_n);
   p.num_tiles = int(tiles_m * tiles_n);
+  {
+    // the last partial round of pair tiles: its tiles become two half-width items each
+    const int rest = plan.split > 1 ? p.num_tiles % plan.conc : 0;
+    p.tail_split = rest > 0 ? plan.split : 1;
+    p.tail_start = p.num_tiles - (p.tail_split > 1 ? rest : 0);
+    p.num_work = p.tail_start + (p.num_tiles - p.tail_start) * p.tail_split;
+  }
   p.num_kb = int((K * es + 127) / 128);
   p.raster = plan.raster;
   p.A = A;
@@ -312,12 +335,15 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     return GEMM_ERR_DRIVER;
   if (p.b_tma) {
     bool ok;
-    if (layout == GEMM_B_K_MAJOR)
+    if (layout == GEMM_B_K_MAJOR) {
       ok = encode_2d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, bk,
                      uint32_t(plan.pair ? bn / 2 : bn));
-    else
+      if (ok && plan.pair && p.tail_split > 1)
+        ok = encode_2d(&L.tmB_half, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, bk, uint32_t(bn / 4));
+    } else {
       ok = encode_2d(&L.tmB, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, 128 / es, bk,
                      es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (!ok) return GEMM_ERR_DRIVER;
   }
   L.b_kmajor = kmajor;
@@ -330,6 +356,9 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   cudaError_t e = kind == KIND_TF32 ? launch_tf32(L) : kind == KIND_BF16 ? launch_bf16(L) : launch_f16(L);
   if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  const int32_t info[8] = {plan.pair ? 2 : 1, bn, p.raster, L.grid, p.tail_split, plan.conc, p.tail_start,
+                           p.num_work};
+  memcpy(t_last_plan, info, sizeof(info));
   return GEMM_OK;
 }
 
@@ -408,8 +437,14 @@ int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns) {
 
 uint64_t gemm_launch_count(void) { return dgt::g_launches.load(); }
 
-int gemm_set_tuning(int variant, int tile_n, int raster) {
-  if (variant < 0 || variant > 2 || raster < 0) return GEMM_ERR_INVALID_VALUE;
+int gemm_last_plan(int32_t* out) {
+  if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
+  memcpy(out, dgt::t_last_plan, sizeof(dgt::t_last_plan));
+  return GEMM_OK;
+}
+
+int gemm_set_tuning(int variant, int tile_n, int raster, int tail_split) {
+  if (variant < 0 || variant > 2 || raster < 0 || tail_split < 0 || tail_split > 2) return GEMM_ERR_INVALID_VALUE;
   if (tile_n != 0) {
     bool ok = false;
     if (variant != 2)
@@ -421,6 +456,7 @@ int gemm_set_tuning(int variant, int tile_n, int raster) {
   dgt::g_force_variant.store(variant);
   dgt::g_force_bn.store(tile_n);
   dgt::g_force_raster.store(raster);
+  dgt::g_force_split.store(tail_split);
   return GEMM_OK;
 }
 

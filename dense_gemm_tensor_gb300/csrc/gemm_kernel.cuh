@@ -79,6 +79,10 @@ struct GemmParams {
   int M, N, K;
   int tiles_m, tiles_n, num_tiles, num_kb;
   int raster;  // band height (in tiles along M) of the tile order
+  // Work items: tiles [0, tail_start) in tile order at full width; the tiles
+  // from tail_start on are each split into tail_split column slices (the last
+  // partial round of tiles spread over more SMs). num_work counts the items.
+  int tail_start, tail_split, num_work;
   const void* A;
   long long lda;
   const void* B;

@@ -62,15 +62,34 @@ struct PairCfg {
   static_assert(ACC_BUFS * BN <= 512, "tensor memory");
   static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
   static_assert(STAGES >= 3, "pipeline depth");
-  static constexpr uint32_t IDESC = (1u << 4) | (KindTraits<KIND>::fmt << 7) | (KindTraits<KIND>::fmt << 10) |
-                                    ((B_KMAJOR ? 0u : 1u) << 16) | (uint32_t(BN >> 3) << 17) |
-                                    (uint32_t(BMP >> 4) << 24);
+  // Instruction descriptor without N (set per work item: BN, or BN / tail_split).
+  static constexpr uint32_t IDESC_NO_N = (1u << 4) | (KindTraits<KIND>::fmt << 7) |
+                                         (KindTraits<KIND>::fmt << 10) | ((B_KMAJOR ? 0u : 1u) << 16) |
+                                         (uint32_t(BMP >> 4) << 24);
 };
+
+// Work item w of the pair kernel -> tile rows, first column and width.
+struct PairWork {
+  int mb, col0, width;
+};
+__device__ __forceinline__ PairWork pair_work(const GemmParams& p, int w, int bn) {
+  int t = w, part = 0, width = bn;
+  if (w >= p.tail_start) {
+    const int f = (w - p.tail_start) / p.tail_split;
+    part = w - p.tail_start - f * p.tail_split;
+    t = p.tail_start + f;
+    width = bn / p.tail_split;
+  }
+  int mb, nb;
+  tile_coords(p, t, mb, nb);
+  return PairWork{mb, nb * bn + part * width, width};
+}
 
 template <int KIND, bool B_KMAJOR, int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmB_half, const GemmParams p) {
+  // tmB_half: K-major B with half-height boxes, for the split work items.
   using Cf = PairCfg<KIND, B_KMAJOR, BN>;
   constexpr int S = Cf::STAGES;
   constexpr int NB = Cf::ACC_BUFS;
@@ -113,6 +132,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (B_KMAJOR && p.tail_split > 1) tma_prefetch_desc(&tmB_half);
   }
   if (warp == 5) {
     tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), Cf::TMEM_COLS);
@@ -129,11 +149,12 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0 && !(p.debug & DEBUG_STALL_PRODUCER)) {
       int it = 0;
       bool ok = true;
-      for (int t = pair; ok && t < p.num_tiles; t += npairs) {
-        int mb, nb;
-        tile_coords(p, t, mb, nb);
-        const int row0 = mb * Cf::BMP + int(rank) * Cf::BM;
-        const int col0 = nb * BN + int(rank) * Cf::BNH;
+      for (int w = pair; ok && w < p.num_work; w += npairs) {
+        const PairWork wk = pair_work(p, w, BN);
+        const int half = wk.width / 2;  // B columns this CTA loads
+        const int row0 = wk.mb * Cf::BMP + int(rank) * Cf::BM;
+        const int col0 = wk.col0 + int(rank) * half;
+        const uint32_t tx = 2u * (Cf::A_BYTES + half * 128u);
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -141,16 +162,18 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_BYTES);
+          if (leader) mbar_arrive_expect_tx(full0 + 8 * s, tx);
           const uint32_t fb = mapa_shared(full0 + 8 * s, 0);
           tma_load_2d_pair(sA + s * Cf::A_BYTES, &tmA, fb, kb * Cf::BK, row0);
           if constexpr (B_KMAJOR) {
-            tma_load_2d_pair(sB + s * Cf::B_BYTES, &tmB, fb, kb * Cf::BK, col0);
+            tma_load_2d_pair(sB + s * Cf::B_BYTES, half == Cf::BNH ? &tmB : &tmB_half, fb, kb * Cf::BK, col0);
           } else {
+            const int nbox = half / Cf::BOXN;
 #pragma unroll
             for (int j = 0; j < Cf::NBOX; ++j)
-              tma_load_2d_pair(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, col0 + j * Cf::BOXN,
-                               kb * Cf::BK);
+              if (j < nbox)
+                tma_load_2d_pair(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, col0 + j * Cf::BOXN,
+                                 kb * Cf::BK);
           }
         }
       }
@@ -161,9 +184,10 @@ __global__ void __launch_bounds__(192, 1)
     if (leader && lane == 0) {
       int it = 0, tc = 0;
       bool ok = true;
-      for (int t = pair; ok && t < p.num_tiles; t += npairs, ++tc) {
+      for (int w = pair; ok && w < p.num_work; w += npairs, ++tc) {
         const int b = tc % NB;
         const uint32_t use = (tc / NB) & 1;
+        const uint32_t idesc = Cf::IDESC_NO_N | (uint32_t(pair_work(p, w, BN).width >> 3) << 17);
         if (!wait_phase(p, acce0 + 8 * b, use ^ 1, ROLE_MMA | (0x80u << 8))) break;
         tc_fence_after();
         const uint32_t d = tmem + b * Cf::ACC_COLS;
@@ -187,9 +211,9 @@ __global__ void __launch_bounds__(192, 1)
               bd = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
             const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
             if constexpr (KIND == KIND_TF32)
-              mma_tf32_pair(d, ad, bd, Cf::IDESC, acc);
+              mma_tf32_pair(d, ad, bd, idesc, acc);
             else
-              mma_f16_pair(d, ad, bd, Cf::IDESC, acc);
+              mma_f16_pair(d, ad, bd, idesc, acc);
           }
           mma_commit_pair(empty0 + 8 * s, 0x3);  // both CTAs may refill stage s
         }
@@ -203,16 +227,15 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
     int tc = 0;
-    for (int t = pair; t < p.num_tiles; t += npairs, ++tc) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
+    for (int w = pair; w < p.num_work; w += npairs, ++tc) {
+      const PairWork wk = pair_work(p, w, BN);
       const int b = tc % NB;
       const uint32_t use = (tc / NB) & 1;
       if (!warp_wait_phase(p, accf0 + 8 * b, use, ROLE_EPILOGUE | (b << 8))) break;
       tc_fence_after();
-      const int row = mb * Cf::BMP + int(rank) * Cf::BM + warp * 32 + lane;
+      const int row = wk.mb * Cf::BMP + int(rank) * Cf::BM + warp * 32 + lane;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
-      const int ncols = min(BN, p.N - nb * BN);
+      const int ncols = min(wk.width, p.N - wk.col0);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         if (c * 32 >= ncols) break;  // warp-uniform
@@ -220,7 +243,7 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_wait_ld();
-        store_row_chunk<KIND>(p, row, nb * BN + c * 32, r);
+        store_row_chunk<KIND>(p, row, wk.col0 + c * 32, r);
       }
       tc_fence_before();
       __syncwarp();

@@ -32,7 +32,8 @@ GEMM_ERR_DEVICE_TIMEOUT = 7
 
 # Every symbol the C header declares.
 EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_get_device_status",
-           "gemm_reset_device_status", "gemm_set_debug", "gemm_launch_count", "gemm_set_tuning")
+           "gemm_reset_device_status", "gemm_set_debug", "gemm_launch_count", "gemm_set_tuning",
+           "gemm_last_plan")
 
 _lib = None
 
@@ -67,8 +68,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.gemm_set_debug.restype = ctypes.c_int
     lib.gemm_launch_count.argtypes = []
     lib.gemm_launch_count.restype = u64
-    lib.gemm_set_tuning.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.gemm_set_tuning.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.gemm_set_tuning.restype = ctypes.c_int
+    lib.gemm_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+    lib.gemm_last_plan.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -193,12 +196,22 @@ def set_debug(flags: int = 0, wait_limit_ns: int = 0) -> None:
     load().gemm_set_debug(flags, wait_limit_ns)
 
 
-def set_tuning(variant: int = 0, tile_n: int = 0, raster: int = 0) -> None:
-    """Force the kernel variant (1 single CTA, 2 CTA pair), tile width and
-    band height for later calls (0 = automatic)."""
-    code = load().gemm_set_tuning(int(variant), int(tile_n), int(raster))
+def set_tuning(variant: int = 0, tile_n: int = 0, raster: int = 0, tail_split: int = 0) -> None:
+    """Force the kernel variant (1 single CTA, 2 CTA pair), tile width, band
+    height and tail split (1 never, 2 when possible) for later calls (0 = automatic)."""
+    code = load().gemm_set_tuning(int(variant), int(tile_n), int(raster), int(tail_split))
     if code != GEMM_OK:
         raise GemmError(code, "gemm_set_tuning")
+
+
+PLAN_FIELDS = ("kernel", "tile_n", "raster", "grid", "tail_split", "concurrent_tiles", "tail_start", "work_items")
+
+
+def last_plan() -> dict:
+    """Launch plan of this thread's last product-kernel call (see gemm_last_plan)."""
+    buf = (ctypes.c_int32 * 8)()
+    load().gemm_last_plan(buf)
+    return dict(zip(PLAN_FIELDS, list(buf)))
 
 
 def launch_count() -> int:

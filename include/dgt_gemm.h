@@ -114,16 +114,27 @@ int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns);
 uint64_t gemm_launch_count(void);
 
 /*
+ * The launch plan of the calling host thread's last GEMM call that launched
+ * the product kernel, as 8 integers in out[0..7]: kernel (1 single CTA, 2 CTA
+ * pair), tile width, band height, grid size in CTAs, column slices of the
+ * last partial round (1 or 2), tiles in flight at once, first sliced tile,
+ * number of work items. All zero before the first such call.
+ */
+int gemm_last_plan(int32_t* out);
+
+/*
  * Tuning hook, process-wide, for subsequent calls. `variant`: 0 = chosen per
  * call, 1 = single-CTA kernel (128-row tiles), 2 = CTA-pair kernel (256-row
  * tiles; only when A and B rows are 16-byte aligned, else the single-CTA
  * kernel runs). `tile_n`: output tile width, 256, 224, 192 or 128 for the
  * single-CTA kernel and 256 or 128 for the pair (0 = chosen per call).
  * `raster`: band height of the tile order in tile rows (0 = chosen per call).
+ * `tail_split`: 0 = chosen per call, 1 = never split the last partial round
+ * of pair tiles, 2 = split it into half-width slices where the shape allows.
  * Results do not depend on any of them. Returns GEMM_ERR_INVALID_VALUE for
  * values outside these sets.
  */
-int gemm_set_tuning(int variant, int tile_n, int raster);
+int gemm_set_tuning(int variant, int tile_n, int raster, int tail_split);
 
 #ifdef __cplusplus
 }
