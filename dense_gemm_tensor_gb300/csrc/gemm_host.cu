@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "dgt_gemm.h"
 #include "launch.h"
@@ -156,12 +157,65 @@ int pair_clusters(int dev, int kind, bool kmajor, int bn) {
   return n;
 }
 
+// ---------------------------------------------------------------- workspace
+// Scratch for the split tail of the pair kernel: arrival counters (first
+// kCounterBytes) followed by fp32 partial tiles. One buffer per (device,
+// stream), allocated on first need and grown (never shrunk) when a larger plan
+// needs it, so calls on one stream reuse it and calls on different streams
+// never share it. The counters carry the launch epoch, so they are zeroed once
+// at allocation and never reset between calls.
+constexpr int kMaxTailSegs = 4;
+constexpr size_t kCounterBytes = 1024 * 2 * sizeof(unsigned long long);  // up to 1024 split tiles
+
+size_t workspace_bytes(int split_tiles, int segs, int bn) {
+  return kCounterBytes + size_t(split_tiles) * size_t(segs) * 2u * 128u * size_t(bn) * sizeof(float);
+}
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+std::unordered_map<uint64_t, Workspace> g_ws;
+
+void* stream_workspace(int dev, cudaStream_t stream, size_t bytes) {
+  const uint64_t key = (uint64_t(uint32_t(dev)) << 56) ^ uint64_t(reinterpret_cast<uintptr_t>(stream));
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  Workspace& w = g_ws[key];
+  if (w.bytes >= bytes) return w.ptr;
+  if (w.ptr != nullptr) {
+    cudaFree(w.ptr);  // waits for the device: no kernel can still be using it
+    w.ptr = nullptr;
+    w.bytes = 0;
+  }
+  void* p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cudaMemset(p, 0, kCounterBytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(p);
+    return nullptr;
+  }
+  w.ptr = p;
+  w.bytes = bytes;
+  return p;
+}
+
+void free_workspaces() {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  for (auto& kv : g_ws)
+    if (kv.second.ptr != nullptr) cudaFree(kv.second.ptr);
+  g_ws.clear();
+}
+
 struct TilePlan {
   bool pair;
   int bn;
   int raster;
   int grid;   // CTAs
-  int split;  // pair kernel: column slices per tile of the last partial round (1 or 2)
+  int segs;   // pair kernel: k-slab segments per tile of the last partial round (1 = no split)
   int conc;   // tiles in flight at once (SMs, or co-resident CTA pairs)
 };
 
@@ -211,21 +265,26 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
     const int64_t rows = pair ? 256 : 128;
     const int64_t tiles = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
     const int64_t full = tiles / conc, rest = tiles % conc;
-    // pair kernel: the last partial round may go as half-width slices on twice the pairs
+    // pair kernel: the tiles of the last partial round may be split along K
+    // into `segs` pieces run by different pairs (fp32 partials summed at the end)
     const int fs = g_force_split.load(std::memory_order_relaxed);
-    const bool can_split =
-        fs != 1 && pair && rest > 0 && 2 * rest <= conc && (kmajor || (bn / 4) % atom == 0);
-    const int split = can_split ? 2 : 1;
+    int segs = 1;
+    if (pair && rest > 0 && fs != 1 && kslabs >= 8) {
+      segs = int(conc / rest);
+      if (segs > kMaxTailSegs) segs = kMaxTailSegs;
+      if (segs < 1) segs = 1;
+    }
     const double tile_cost = double(kslabs) * slab_cycles(bn, cols) + 600.0;
     double cost = double(full) * tile_cost;
-    if (rest > 0) cost += split == 2 ? double(kslabs) * slab_cycles(bn / 2, cols / 2) + 600.0 : tile_cost;
+    if (rest > 0) cost += segs > 1 ? tile_cost / segs + 1200.0 : tile_cost;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       const int64_t tiles_m = (M + rows - 1) / rows;
-      const int64_t work = tiles + (split - 1) * rest;
+      const int64_t work = tiles + (segs - 1) * rest;
       const int64_t grid_tiles = work < conc ? work : conc;
-      best = TilePlan{pair, bn, int(tiles_m < 8 ? tiles_m : 8), int(pair ? 2 * grid_tiles : grid_tiles), split,
-                      conc};
+      const int band = pair ? 2 : 8;  // measured best at 4096^3: 1-4 pair rows, 4-8 single-CTA rows
+      best = TilePlan{pair, bn, int(tiles_m < band ? tiles_m : band), int(pair ? 2 * grid_tiles : grid_tiles),
+                      segs, conc};
     }
   };
   for (int bn : kPairTileWidths) consider(true, bn);
@@ -299,15 +358,24 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   p.tiles_m = int(tiles_m);
   p.tiles_n = int(tiles_n);
   p.num_tiles = int(tiles_m * tiles_n);
-  {
-    // the last partial round of pair tiles: its tiles become two half-width items each
-    const int rest = plan.split > 1 ? p.num_tiles % plan.conc : 0;
-    p.tail_split = rest > 0 ? plan.split : 1;
-    p.tail_start = p.num_tiles - (p.tail_split > 1 ? rest : 0);
-    p.num_work = p.tail_start + (p.num_tiles - p.tail_start) * p.tail_split;
-  }
   p.num_kb = int((K * es + 127) / 128);
   p.raster = plan.raster;
+  p.tail_start = p.num_tiles;
+  p.tail_segs = 1;
+  p.num_work = p.num_tiles;
+  if (plan.pair && plan.segs > 1) {
+    // the last partial round of pair tiles: each tile becomes `segs` k-slab segments
+    const int rest = p.num_tiles % plan.conc;
+    const size_t need = workspace_bytes(rest, plan.segs, bn);
+    void* ws = (rest > 0 && rest <= 1024) ? stream_workspace(dev_id, stream, need) : nullptr;
+    if (ws != nullptr) {
+      p.tail_segs = plan.segs;
+      p.tail_start = p.num_tiles - rest;
+      p.num_work = p.tail_start + rest * plan.segs;
+      p.ws_ctr = static_cast<unsigned long long*>(ws);
+      p.ws = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+    }
+  }
   p.A = A;
   p.lda = lda;
   p.B = B;
@@ -338,8 +406,6 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     if (layout == GEMM_B_K_MAJOR) {
       ok = encode_2d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, bk,
                      uint32_t(plan.pair ? bn / 2 : bn));
-      if (ok && plan.pair && p.tail_split > 1)
-        ok = encode_2d(&L.tmB_half, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, bk, uint32_t(bn / 4));
     } else {
       ok = encode_2d(&L.tmB, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, 128 / es, bk,
                      es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
@@ -353,10 +419,14 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   L.threads = (p.a_tma && p.b_tma) ? 192 : 320;
   L.stream = stream;
 
+  // internal consistency of the derived launch parameters (a violation is a library bug)
+  if (p.raster < 1 || p.num_kb < 1 || p.num_tiles < 1 || p.num_work < p.num_tiles || p.tail_segs < 1 ||
+      p.tail_segs > kMaxTailSegs || L.grid < 1 || (L.pair && (L.grid % 2 != 0)) || p.tiles_n < 1 || p.tiles_m < 1)
+    return GEMM_ERR_LAUNCH;
   cudaError_t e = kind == KIND_TF32 ? launch_tf32(L) : kind == KIND_BF16 ? launch_bf16(L) : launch_f16(L);
   if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  const int32_t info[8] = {plan.pair ? 2 : 1, bn, p.raster, L.grid, p.tail_split, plan.conc, p.tail_start,
+  const int32_t info[8] = {plan.pair ? 2 : 1, bn, p.raster, L.grid, p.tail_segs, plan.conc, p.tail_start,
                            p.num_work};
   memcpy(t_last_plan, info, sizeof(info));
   return GEMM_OK;
@@ -436,6 +506,12 @@ int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns) {
 }
 
 uint64_t gemm_launch_count(void) { return dgt::g_launches.load(); }
+
+int gemm_free_workspaces(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_LAUNCH;
+  dgt::free_workspaces();
+  return GEMM_OK;
+}
 
 int gemm_last_plan(int32_t* out) {
   if (out == nullptr) return GEMM_ERR_INVALID_VALUE;

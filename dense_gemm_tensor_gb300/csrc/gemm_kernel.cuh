@@ -79,10 +79,14 @@ struct GemmParams {
   int M, N, K;
   int tiles_m, tiles_n, num_tiles, num_kb;
   int raster;  // band height (in tiles along M) of the tile order
-  // Work items: tiles [0, tail_start) in tile order at full width; the tiles
-  // from tail_start on are each split into tail_split column slices (the last
-  // partial round of tiles spread over more SMs). num_work counts the items.
-  int tail_start, tail_split, num_work;
+  // Work items: tiles [0, tail_start) in tile order, whole; each tile from
+  // tail_start on is split into tail_segs ranges of k-slabs (the last partial
+  // round of tiles spread over more SMs). num_work counts the items. The
+  // segments' fp32 partial tiles meet in `ws`; `ws_ctr` holds one arrival
+  // counter per (split tile, CTA of the pair), tagged with the launch epoch.
+  int tail_start, tail_segs, num_work;
+  float* ws;
+  unsigned long long* ws_ctr;
   const void* A;
   long long lda;
   const void* B;
@@ -303,7 +307,7 @@ __device__ __forceinline__ void store_one(void* C, long long idx, uint32_t bits)
 // 32 accumulator columns of one row -> C[row][col0 .. col0+31].
 template <int KIND>
 __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, int col0, const uint32_t (&r)[32]) {
-  if (row >= p.M || col0 >= p.N) return;
+  if (row < 0 || row >= p.M || col0 < 0 || col0 >= p.N) return;
   const long long idx0 = static_cast<long long>(row) * p.ldc + col0;
   if (p.c_vec && col0 + 32 <= p.N) {
     if constexpr (KIND == KIND_TF32) {
@@ -322,6 +326,32 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, in
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (j < lim) store_one<KIND>(p.C, idx0 + j, r[j]);
+  }
+}
+
+// Reads `nchunks` 32-column chunks of this warp's 32 accumulator rows from
+// tensor memory and hands each to `use(c, r)`, keeping the next chunk's load
+// in flight while the current one is used. Warp-collective.
+template <typename Use>
+__device__ __forceinline__ void for_each_acc_chunk(uint32_t taddr, int nchunks, Use use) {
+  uint32_t ra[32], rb[32];
+  __syncwarp();
+  tmem_ld_32x32b_x32(taddr, ra);
+  tmem_wait_ld_into(ra);
+#pragma unroll 1
+  for (int c = 0; c < nchunks; c += 2) {
+    __syncwarp();
+    if (c + 1 < nchunks) tmem_ld_32x32b_x32(taddr + (c + 1) * 32, rb);
+    use(c, ra);
+    __syncwarp();
+    tmem_wait_ld_into(rb);
+    if (c + 1 < nchunks) {
+      __syncwarp();
+      if (c + 2 < nchunks) tmem_ld_32x32b_x32(taddr + (c + 2) * 32, ra);
+      use(c + 1, rb);
+      __syncwarp();
+      tmem_wait_ld_into(ra);
+    }
   }
 }
 
@@ -470,15 +500,8 @@ __global__ void __launch_bounds__(320, 1)
       const int row = mb * Cf::BM + warp * 32 + lane;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
       const int ncols = min(Cf::BN, p.N - nb * Cf::BN);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        if (c * 32 >= ncols) break;  // warp-uniform
-        uint32_t r[32];
-        __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane stores
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
-        tmem_wait_ld();
-        store_row_chunk<KIND>(p, row, nb * Cf::BN + c * 32, r);
-      }
+      for_each_acc_chunk(taddr, (ncols + 31) / 32,
+                         [&](int c, const uint32_t(&r)[32]) { store_row_chunk<KIND>(p, row, nb * Cf::BN + c * 32, r); });
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * b);

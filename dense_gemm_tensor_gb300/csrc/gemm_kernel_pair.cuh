@@ -9,6 +9,14 @@
 // both CTAs' shared memory at the same offsets and leaves rows 0-127 of the
 // accumulator in the leader's tensor memory and rows 128-255 in the peer's.
 //
+// Tail: when the tiles do not fill a whole number of rounds of the grid, each
+// tile of the last partial round is split into `tail_segs` ranges of k-slabs
+// run by different pairs, so the round takes 1/tail_segs of a tile's time.
+// Every segment writes its fp32 partial tile to the workspace and bumps an
+// arrival counter; the last to arrive sums the segments in segment order
+// (its own from tensor memory) and stores C. No CTA waits for another, and
+// the sum does not depend on the arrival order.
+//
 // Synchronisation:
 //   full[s]   leader only; 1 arrival (leader producer, expecting the bytes of
 //             both CTAs' TMA loads, which all complete on this barrier)
@@ -19,12 +27,6 @@
 #pragma once
 
 #include "gemm_kernel.cuh"
-
-// Accumulator buffers per CTA (1: the epilogue and the next tile's k-loop
-// alternate; 2: they overlap).
-#ifndef DGT_PAIR_ACC_BUFS
-#define DGT_PAIR_ACC_BUFS 2
-#endif
 
 namespace dgt {
 
@@ -52,44 +54,68 @@ struct PairCfg {
   static constexpr int RESERVED = 1024 + 256;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int ACC_BUFS = DGT_PAIR_ACC_BUFS;
+  static constexpr int ACC_BUFS = 2;  // the epilogue of one tile overlaps the next tile's k-loop
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = (ACC_BUFS * BN <= 256) ? 256 : 512;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + RESERVED;
+  static constexpr int PARTIAL_FLOATS = BM * BN;  // one CTA's fp32 partial tile
   static_assert(B_KMAJOR || NBOX * BOXN == BNH, "MN-major B: each CTA's half must be whole 128-byte slabs");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
   static_assert(ACC_BUFS * BN <= 512, "tensor memory");
-  static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
+  static_assert(NUM_BARS * 8 + 32 <= 256, "barrier area");
   static_assert(STAGES >= 3, "pipeline depth");
-  // Instruction descriptor without N (set per work item: BN, or BN / tail_split).
-  static constexpr uint32_t IDESC_NO_N = (1u << 4) | (KindTraits<KIND>::fmt << 7) |
-                                         (KindTraits<KIND>::fmt << 10) | ((B_KMAJOR ? 0u : 1u) << 16) |
-                                         (uint32_t(BMP >> 4) << 24);
+  static constexpr uint32_t IDESC = (1u << 4) | (KindTraits<KIND>::fmt << 7) | (KindTraits<KIND>::fmt << 10) |
+                                    ((B_KMAJOR ? 0u : 1u) << 16) | (uint32_t(BN >> 3) << 17) |
+                                    (uint32_t(BMP >> 4) << 24);
 };
 
-// Work item w of the pair kernel -> tile rows, first column and width.
+// Work item w of the pair kernel -> tile, k-slab range and (for split tiles)
+// the tail index f and segment.
 struct PairWork {
-  int mb, col0, width;
+  int mb, nb, kb0, kb1, f, seg;
 };
-__device__ __forceinline__ PairWork pair_work(const GemmParams& p, int w, int bn) {
-  int t = w, part = 0, width = bn;
+__device__ __forceinline__ PairWork pair_work(const GemmParams& p, int w) {
+  PairWork r;
+  int t = w;
+  r.f = -1;
+  r.seg = 0;
+  r.kb0 = 0;
+  r.kb1 = p.num_kb;
   if (w >= p.tail_start) {
-    const int f = (w - p.tail_start) / p.tail_split;
-    part = w - p.tail_start - f * p.tail_split;
-    t = p.tail_start + f;
-    width = bn / p.tail_split;
+    const int j = w - p.tail_start;
+    r.f = j / p.tail_segs;
+    r.seg = j - r.f * p.tail_segs;
+    t = p.tail_start + r.f;
+    r.kb0 = static_cast<int>((static_cast<long long>(p.num_kb) * r.seg) / p.tail_segs);
+    r.kb1 = static_cast<int>((static_cast<long long>(p.num_kb) * (r.seg + 1)) / p.tail_segs);
   }
-  int mb, nb;
-  tile_coords(p, t, mb, nb);
-  return PairWork{mb, nb * bn + part * width, width};
+  tile_coords(p, t, r.mb, r.nb);
+  return r;
 }
+
+// Registers an arrival on a split tile's counter and returns the arrival
+// index (0-based) within this launch. The counter holds (epoch << 32) | count,
+// so a value left by an earlier launch reads as zero arrivals.
+__device__ __forceinline__ int arrive_split(const GemmParams& p, unsigned long long* ctr) {
+  const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
+  unsigned long long cur = atomicAdd(ctr, 0ull);
+  for (int guard = 0; guard < (1 << 20); ++guard) {
+    const unsigned long long cnt = ((cur & 0xFFFFFFFF00000000ull) == tag) ? (cur & 0xFFFFFFFFull) : 0ull;
+    const unsigned long long seen = atomicCAS(ctr, cur, tag | (cnt + 1));
+    if (seen == cur) return static_cast<int>(cnt);
+    cur = seen;
+  }
+  record_timeout(p, ROLE_EPILOGUE | (0xF0u << 8));
+  return 0;
+}
+
+__device__ __forceinline__ void epilogue_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <int KIND, bool B_KMAJOR, int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmB_half, const GemmParams p) {
-  // tmB_half: K-major B with half-height boxes, for the split work items.
+                     const GemmParams p) {
   using Cf = PairCfg<KIND, B_KMAJOR, BN>;
   constexpr int S = Cf::STAGES;
   constexpr int NB = Cf::ACC_BUFS;
@@ -109,6 +135,8 @@ __global__ void __launch_bounds__(192, 1)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + Cf::NUM_BARS);
   volatile int* issued_slot = reinterpret_cast<volatile int*>(bars + Cf::NUM_BARS) + 1;
   volatile int* consumed_slot = reinterpret_cast<volatile int*>(bars + Cf::NUM_BARS) + 2;
+  volatile int* last_slot = reinterpret_cast<volatile int*>(bars + Cf::NUM_BARS) + 3;
+  volatile int* ok_slot = reinterpret_cast<volatile int*>(bars + Cf::NUM_BARS) + 4;  // [2]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -132,7 +160,6 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (B_KMAJOR && p.tail_split > 1) tma_prefetch_desc(&tmB_half);
   }
   if (warp == 5) {
     tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), Cf::TMEM_COLS);
@@ -150,30 +177,26 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0;
       bool ok = true;
       for (int w = pair; ok && w < p.num_work; w += npairs) {
-        const PairWork wk = pair_work(p, w, BN);
-        const int half = wk.width / 2;  // B columns this CTA loads
+        const PairWork wk = pair_work(p, w);
         const int row0 = wk.mb * Cf::BMP + int(rank) * Cf::BM;
-        const int col0 = wk.col0 + int(rank) * half;
-        const uint32_t tx = 2u * (Cf::A_BYTES + half * 128u);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const int col0 = wk.nb * BN + int(rank) * Cf::BNH;
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!wait_phase(p, empty0 + 8 * s, ph ^ 1, ROLE_PRODUCER | (s << 8))) {
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(full0 + 8 * s, tx);
+          if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_BYTES);
           const uint32_t fb = mapa_shared(full0 + 8 * s, 0);
           tma_load_2d_pair(sA + s * Cf::A_BYTES, &tmA, fb, kb * Cf::BK, row0);
           if constexpr (B_KMAJOR) {
-            tma_load_2d_pair(sB + s * Cf::B_BYTES, half == Cf::BNH ? &tmB : &tmB_half, fb, kb * Cf::BK, col0);
+            tma_load_2d_pair(sB + s * Cf::B_BYTES, &tmB, fb, kb * Cf::BK, col0);
           } else {
-            const int nbox = half / Cf::BOXN;
 #pragma unroll
             for (int j = 0; j < Cf::NBOX; ++j)
-              if (j < nbox)
-                tma_load_2d_pair(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, col0 + j * Cf::BOXN,
-                                 kb * Cf::BK);
+              tma_load_2d_pair(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, col0 + j * Cf::BOXN,
+                               kb * Cf::BK);
           }
         }
       }
@@ -185,13 +208,13 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0, tc = 0;
       bool ok = true;
       for (int w = pair; ok && w < p.num_work; w += npairs, ++tc) {
+        const PairWork wk = pair_work(p, w);
         const int b = tc % NB;
         const uint32_t use = (tc / NB) & 1;
-        const uint32_t idesc = Cf::IDESC_NO_N | (uint32_t(pair_work(p, w, BN).width >> 3) << 17);
         if (!wait_phase(p, acce0 + 8 * b, use ^ 1, ROLE_MMA | (0x80u << 8))) break;
         tc_fence_after();
         const uint32_t d = tmem + b * Cf::ACC_COLS;
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!wait_phase(p, full0 + 8 * s, ph, ROLE_MMA | (s << 8))) {
@@ -209,11 +232,11 @@ __global__ void __launch_bounds__(192, 1)
               bd = sdesc(b_addr + kk * 32, 16, 1024, SWZ_128B);
             else
               bd = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
-            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t acc = (kb > wk.kb0 || kk > 0) ? 1u : 0u;
             if constexpr (KIND == KIND_TF32)
-              mma_tf32_pair(d, ad, bd, idesc, acc);
+              mma_tf32_pair(d, ad, bd, Cf::IDESC, acc);
             else
-              mma_f16_pair(d, ad, bd, idesc, acc);
+              mma_f16_pair(d, ad, bd, Cf::IDESC, acc);
           }
           mma_commit_pair(empty0 + 8 * s, 0x3);  // both CTAs may refill stage s
         }
@@ -226,24 +249,101 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
+    // The four warps take every decision together (thread 0 waits, the named
+    // barrier publishes the outcome), so the barriers below always see all 128.
+    const int tid = threadIdx.x;  // 0..127
     int tc = 0;
     for (int w = pair; w < p.num_work; w += npairs, ++tc) {
-      const PairWork wk = pair_work(p, w, BN);
+      const PairWork wk = pair_work(p, w);
       const int b = tc % NB;
       const uint32_t use = (tc / NB) & 1;
-      if (!warp_wait_phase(p, accf0 + 8 * b, use, ROLE_EPILOGUE | (b << 8))) break;
+      if (tid == 0) ok_slot[tc & 1] = wait_phase(p, accf0 + 8 * b, use, ROLE_EPILOGUE | (b << 8)) ? 1 : 0;
+      epilogue_barrier();
+      if (!ok_slot[tc & 1]) break;
       tc_fence_after();
       const int row = wk.mb * Cf::BMP + int(rank) * Cf::BM + warp * 32 + lane;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
-      const int ncols = min(wk.width, p.N - wk.col0);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        if (c * 32 >= ncols) break;  // warp-uniform
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
-        tmem_wait_ld();
-        store_row_chunk<KIND>(p, row, wk.col0 + c * 32, r);
+      const int ncols = min(BN, p.N - wk.nb * BN);
+      const int nchunks = (ncols + 31) / 32;
+      const int col0 = wk.nb * BN;
+      if (wk.f < 0) {
+        for_each_acc_chunk(taddr, nchunks,
+                           [&](int c, const uint32_t(&r)[32]) { store_row_chunk<KIND>(p, row, col0 + c * 32, r); });
+      } else {
+        // split tile: publish this segment's partial, then find out whether it is the last
+        float4* mine = reinterpret_cast<float4*>(
+            p.ws + (static_cast<long long>(wk.f * p.tail_segs + wk.seg) * 2 + rank) * Cf::PARTIAL_FLOATS);
+        for_each_acc_chunk(taddr, nchunks, [&](int c, const uint32_t(&r)[32]) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            __stcg(mine + (c * 8 + q) * 128 + tid,
+                   make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+        });
+        __threadfence();
+        epilogue_barrier();
+        if (tid == 0) {
+          const int arrival = arrive_split(p, p.ws_ctr + wk.f * 2 + rank);
+          *last_slot = (arrival + 1 == p.tail_segs) ? 1 : 0;
+        }
+        epilogue_barrier();
+        const bool last = *last_slot != 0;
+        __threadfence();
+        if (last && p.tail_segs == 2) {
+          // C = own + other: fp32 addition commutes, so which segment arrives last does not matter
+          const float4* other = reinterpret_cast<const float4*>(
+              p.ws + (static_cast<long long>(wk.f * 2 + (1 - wk.seg)) * 2 + rank) * Cf::PARTIAL_FLOATS);
+          float4 nxt[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) nxt[q] = __ldcg(other + q * 128 + tid);
+          for_each_acc_chunk(taddr, nchunks, [&](int c, const uint32_t(&r)[32]) {
+            float4 cur[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) cur[q] = nxt[q];
+            if (c + 1 < nchunks) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) nxt[q] = __ldcg(other + ((c + 1) * 8 + q) * 128 + tid);
+            }
+            uint32_t sum[32];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              sum[4 * q] = __float_as_uint(__uint_as_float(r[4 * q]) + cur[q].x);
+              sum[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) + cur[q].y);
+              sum[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + cur[q].z);
+              sum[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + cur[q].w);
+            }
+            store_row_chunk<KIND>(p, row, col0 + c * 32, sum);
+          });
+        } else if (last) {
+          // three or four segments: add them in segment order; this CTA's own one comes from tensor memory
+          for_each_acc_chunk(taddr, nchunks, [&](int c, const uint32_t(&r)[32]) {
+            float acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+            for (int sg = 0; sg < p.tail_segs; ++sg) {
+              if (sg == wk.seg) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  acc[j] = (sg == 0) ? __uint_as_float(r[j]) : acc[j] + __uint_as_float(r[j]);
+              } else {
+                const float4* part = reinterpret_cast<const float4*>(
+                    p.ws + (static_cast<long long>(wk.f * p.tail_segs + sg) * 2 + rank) * Cf::PARTIAL_FLOATS);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float4 v = __ldcg(part + (c * 8 + q) * 128 + tid);
+                  acc[4 * q] = (sg == 0) ? v.x : acc[4 * q] + v.x;
+                  acc[4 * q + 1] = (sg == 0) ? v.y : acc[4 * q + 1] + v.y;
+                  acc[4 * q + 2] = (sg == 0) ? v.z : acc[4 * q + 2] + v.z;
+                  acc[4 * q + 3] = (sg == 0) ? v.w : acc[4 * q + 3] + v.w;
+                }
+              }
+            }
+            uint32_t out[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) out[j] = __float_as_uint(acc[j]);
+            store_row_chunk<KIND>(p, row, col0 + c * 32, out);
+          });
+        }
       }
       tc_fence_before();
       __syncwarp();

@@ -12,7 +12,6 @@ namespace dgt {
 struct LaunchPlan {
   CUtensorMap tmA;  // valid when p.a_tma
   CUtensorMap tmB;  // valid when p.b_tma
-  CUtensorMap tmB_half;  // pair kernel, K-major B: half-height boxes for split work items
   GemmParams p;
   bool b_kmajor;
   bool pair;  // CTA-pair kernel (cluster of 2, cta_group::2)
@@ -90,7 +89,7 @@ cudaError_t launch_pair_variant(const LaunchPlan& L) {
   cfg.stream = L.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmB_half, L.p);
+  e = cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -33,7 +33,7 @@ GEMM_ERR_DEVICE_TIMEOUT = 7
 # Every symbol the C header declares.
 EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_get_device_status",
            "gemm_reset_device_status", "gemm_set_debug", "gemm_launch_count", "gemm_set_tuning",
-           "gemm_last_plan")
+           "gemm_last_plan", "gemm_free_workspaces")
 
 _lib = None
 
@@ -72,6 +72,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.gemm_set_tuning.restype = ctypes.c_int
     lib.gemm_last_plan.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.gemm_last_plan.restype = ctypes.c_int
+    lib.gemm_free_workspaces.argtypes = []
+    lib.gemm_free_workspaces.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -204,7 +206,7 @@ def set_tuning(variant: int = 0, tile_n: int = 0, raster: int = 0, tail_split: i
         raise GemmError(code, "gemm_set_tuning")
 
 
-PLAN_FIELDS = ("kernel", "tile_n", "raster", "grid", "tail_split", "concurrent_tiles", "tail_start", "work_items")
+PLAN_FIELDS = ("kernel", "tile_n", "raster", "grid", "tail_segs", "concurrent_tiles", "tail_start", "work_items")
 
 
 def last_plan() -> dict:
@@ -212,6 +214,13 @@ def last_plan() -> dict:
     buf = (ctypes.c_int32 * 8)()
     load().gemm_last_plan(buf)
     return dict(zip(PLAN_FIELDS, list(buf)))
+
+
+def free_workspaces() -> None:
+    """Release the scratch buffers the library holds (waits for the device)."""
+    code = load().gemm_free_workspaces()
+    if code != GEMM_OK:
+        raise GemmError(code, "gemm_free_workspaces")
 
 
 def launch_count() -> int:

@@ -28,10 +28,19 @@
  *   run to run (no atomics).
  *
  * Ownership and memory: every pointer is device memory (or managed memory) of
- * the current CUDA device, owned by the caller. The library allocates nothing
- * per call; it keeps, per device, two status words in its own module memory.
- * C is fully overwritten and must not overlap A or B. Elements beyond the
- * logical row length (columns >= K, >= N) are never read or written.
+ * the current CUDA device, owned by the caller. C is fully overwritten and
+ * must not overlap A or B. Elements beyond the logical row length (columns
+ * >= K, >= N) are never read or written. The library keeps, per device, two
+ * status words in its own module memory, and per (device, stream) one scratch
+ * buffer for split tiles (see below): the first call on a stream whose shape
+ * splits tiles allocates it with cudaMalloc (make that first call outside
+ * stream capture), and it is reused by later calls on that stream, grown
+ * only when a larger split needs more, and released by gemm_free_workspaces.
+ *
+ * Split tiles: when the output tiles do not fill a whole number of rounds of
+ * the GPU, each tile of the last partial round may be computed as 2-4 ranges
+ * of K by different SM pairs whose fp32 partial sums are added at the end
+ * (in a fixed order: results stay deterministic run to run).
  *
  * Degenerate shapes: M = 0 or N = 0 does nothing; K = 0 writes C = 0.
  *
@@ -110,15 +119,18 @@ int gemm_reset_device_status(void);
  */
 int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns);
 
+/* Waits for the device, then frees every scratch buffer the library holds. */
+int gemm_free_workspaces(void);
+
 /* Number of kernels this library has launched in this process. */
 uint64_t gemm_launch_count(void);
 
 /*
  * The launch plan of the calling host thread's last GEMM call that launched
  * the product kernel, as 8 integers in out[0..7]: kernel (1 single CTA, 2 CTA
- * pair), tile width, band height, grid size in CTAs, column slices of the
- * last partial round (1 or 2), tiles in flight at once, first sliced tile,
- * number of work items. All zero before the first such call.
+ * pair), tile width, band height, grid size in CTAs, K segments per tile of
+ * the last partial round (1 = not split), tiles in flight at once, first
+ * split tile, number of work items. All zero before the first such call.
  */
 int gemm_last_plan(int32_t* out);
 
@@ -129,8 +141,8 @@ int gemm_last_plan(int32_t* out);
  * kernel runs). `tile_n`: output tile width, 256, 224, 192 or 128 for the
  * single-CTA kernel and 256 or 128 for the pair (0 = chosen per call).
  * `raster`: band height of the tile order in tile rows (0 = chosen per call).
- * `tail_split`: 0 = chosen per call, 1 = never split the last partial round
- * of pair tiles, 2 = split it into half-width slices where the shape allows.
+ * `tail_split`: 0 or 2 = split the tiles of the last partial round along K
+ * where the shape allows (the default), 1 = never split.
  * Results do not depend on any of them. Returns GEMM_ERR_INVALID_VALUE for
  * values outside these sets.
  */

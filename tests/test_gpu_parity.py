@@ -96,7 +96,7 @@ def test_small_shapes_full(dtype, layout, shape):
 def test_every_tile_width_full(dtype, layout, tile_n):
     """Each built tile width, forced, on a ragged multi-tile shape (TMA path)
     and on an odd-pitch shape (copy-warp path)."""
-    gemm.set_tuning(1, tile_n, 3)
+    gemm.set_tuning(1, tile_n, 3, 0)
     try:
         for (M, N, K, lda, ldb) in [(300, 700, 520, 520, None), (260, 450, 300, 301, 451)]:
             if ldb is None:
@@ -108,7 +108,7 @@ def test_every_tile_width_full(dtype, layout, tile_n):
             C, _ = _run(p)
             _check_full(p, C)
     finally:
-        gemm.set_tuning(0, 0, 0)
+        gemm.set_tuning(0, 0, 0, 0)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
@@ -118,7 +118,7 @@ def test_pair_kernel_full(dtype, layout, tile_n):
     """The CTA-pair kernel (256-row tiles over two SMs), forced, on shapes
     with a ragged pair-row (M = 129: the second CTA's rows are all past M),
     ragged columns and several waves of tiles."""
-    gemm.set_tuning(2, tile_n, 2)
+    gemm.set_tuning(2, tile_n, 2, 0)
     try:
         for (M, N, K) in [(300, 700, 520), (129, 300, 200), (1000, 1500, 336), (2048, 1024, 64)]:
             ldb = N if layout == 0 else K
@@ -130,7 +130,33 @@ def test_pair_kernel_full(dtype, layout, tile_n):
             _check_full(p, C)
             assert torch.all(Cbuf[:, N:] == 3.0)
     finally:
-        gemm.set_tuning(0, 0, 0)
+        gemm.set_tuning(0, 0, 0, 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "tf32"])
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("shape", [(768, 2560, 1000), (1280, 1024, 1000), (768, 1024, 1000), (4096, 4096, 512)])
+def test_pair_split_tail(dtype, layout, shape):
+    """Tiles of the last partial round split along K (2-4 segments, chosen
+    from the co-resident pair count): full parity, and bitwise-equal results
+    over repeated runs whatever segment arrives last."""
+    M, N, K = shape
+    gemm.set_tuning(2, 256, 0, 0)
+    try:
+        p = inputs.make_problem("split", dtype, M, N, K, layout=layout, seed_a=M + N, seed_b=K, dist_a="normal")
+        C1, _ = _run(p)
+        plan = gemm.last_plan()
+        assert plan["kernel"] == 2
+        tiles = -(-M // 256) * -(-N // 256)
+        if tiles % plan["concurrent_tiles"]:
+            assert plan["tail_segs"] > 1, plan
+        assert plan["work_items"] == plan["tail_start"] + (tiles - plan["tail_start"]) * plan["tail_segs"]
+        _check_full(p, C1)
+        for _ in range(2):
+            C2, _ = _run(p)
+            assert torch.equal(C1, C2)
+    finally:
+        gemm.set_tuning(0, 0, 0, 0)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
@@ -219,13 +245,13 @@ def test_wait_time_limit_reports_and_recovers(variant):
     C = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
     gemm.reset_device_status()
     gemm.set_debug(1, 20_000_000)  # 20 ms
-    gemm.set_tuning(variant, 0, 0)
+    gemm.set_tuning(variant, 0, 0, 0)
     try:
         gemm.matmul(A, B, C)
         word = gemm.device_status()
     finally:
         gemm.set_debug(0, 0)
-        gemm.set_tuning(0, 0, 0)
+        gemm.set_tuning(0, 0, 0, 0)
     assert word & 0xF == 1
     # the MMA issuer (2) or the epilogue (3) runs out first; both wait on the stalled pipeline
     assert (word >> 4) & 0xF in (2, 3)
