@@ -165,7 +165,7 @@ int pair_clusters(int dev, int kind, bool kmajor, int bn) {
 // never share it. The counters carry the launch epoch, so they are zeroed once
 // at allocation and never reset between calls.
 constexpr int kMaxTailSegs = 4;
-constexpr size_t kCounterBytes = 1024 * 2 * sizeof(unsigned long long);  // up to 1024 split tiles
+constexpr size_t kCounterBytes = kSplitCounterBytes;  // up to 1024 split tiles
 
 size_t workspace_bytes(int split_tiles, int segs, int bn) {
   return kCounterBytes + size_t(split_tiles) * size_t(segs) * 2u * 128u * size_t(bn) * sizeof(float);
@@ -298,7 +298,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
 }
 
 int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-             void* C, int64_t ldc, int layout, void* stream_ptr) {
+             void* C, int64_t ldc, int layout, void* stream_ptr, const ExternalScratch* ext = nullptr) {
   const int es = (kind == KIND_TF32) ? 4 : 2;
   const int64_t kLim = (int64_t(1) << 31) - 1;
   if (M < 0 || N < 0 || K < 0 || M > kLim || N > kLim || K > kLim) return GEMM_ERR_INVALID_VALUE;
@@ -367,7 +367,13 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     // the last partial round of pair tiles: each tile becomes `segs` k-slab segments
     const int rest = p.num_tiles % plan.conc;
     const size_t need = workspace_bytes(rest, plan.segs, bn);
-    void* ws = (rest > 0 && rest <= 1024) ? stream_workspace(dev_id, stream, need) : nullptr;
+    void* ws = nullptr;
+    if (ext != nullptr) {
+      if (rest > 1024 || need > ext->bytes) return GEMM_ERR_SCRATCH_LIMIT;
+      ws = ext->ptr;
+    } else if (rest > 0 && rest <= 1024) {
+      ws = stream_workspace(dev_id, stream, need);
+    }
     if (ws != nullptr) {
       p.tail_segs = plan.segs;
       p.tail_start = p.num_tiles - rest;
@@ -434,6 +440,11 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
 
 }  // namespace
 
+int run_gemm_external(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                      int64_t ldb, void* C, int64_t ldc, int layout, void* stream, const ExternalScratch* ext) {
+  return run_gemm(kind, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, ext);
+}
+
 cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count) {
   const long long total = static_cast<long long>(M) * N;
   long long blocks = (total + 255) / 256;
@@ -474,6 +485,7 @@ const char* gemm_status_string(int status) {
     case GEMM_ERR_NOT_DEVICE_MEMORY: return "pointer is not device memory of the current device";
     case GEMM_ERR_DRIVER: return "tensor-map encoding failed in the CUDA driver";
     case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel exceeded its wait time limit and gave up";
+    case GEMM_ERR_SCRATCH_LIMIT: return "the shape needs more scratch than the fixed scratch array holds";
     default: return "unknown status";
   }
 }

@@ -29,6 +29,22 @@ int pair_clusters_bf16(bool kmajor, int bn);
 int pair_clusters_tf32(bool kmajor, int bn);
 cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count);
 
+// Split-tail scratch layout: arrival counters for up to 1024 split tiles,
+// then the fp32 partial tiles.
+constexpr size_t kSplitCounterBytes = 1024 * 2 * sizeof(unsigned long long);
+
+// Caller-owned scratch for the split tail (instead of the per-stream buffer
+// the library allocates): device address and capacity in bytes.
+struct ExternalScratch {
+  void* ptr;
+  size_t bytes;
+};
+
+// The C entry points' common body; `ext` non-null: take the split-tail
+// scratch from `ext` and refuse plans that need more than it holds.
+int run_gemm_external(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                      int64_t ldb, void* C, int64_t ldc, int layout, void* stream, const ExternalScratch* ext);
+
 // Tile widths the kernels are built for (the host picks one per call).
 constexpr int kTileWidths[] = {256, 224, 192, 128};
 constexpr int kPairTileWidths[] = {256, 128};

@@ -29,11 +29,12 @@ GEMM_ERR_LAUNCH = 4
 GEMM_ERR_NOT_DEVICE_MEMORY = 5
 GEMM_ERR_DRIVER = 6
 GEMM_ERR_DEVICE_TIMEOUT = 7
+GEMM_ERR_SCRATCH_LIMIT = 8
 
 # Every symbol the C header declares.
 EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_get_device_status",
            "gemm_reset_device_status", "gemm_set_debug", "gemm_launch_count", "gemm_set_tuning",
-           "gemm_last_plan", "gemm_free_workspaces")
+           "gemm_last_plan", "gemm_free_workspaces", "gemm_bf16_static_scratch")
 
 _lib = None
 
@@ -54,7 +55,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         raise RuntimeError(f"{path} is missing: build it with dense_gemm_tensor_gb300.build.build()")
     lib = ctypes.CDLL(path)
     i64, vp, u32, u64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64
-    for name in ("gemm_tf32", "gemm_f16", "gemm_bf16"):
+    for name in ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_bf16_static_scratch"):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, vp]
         fn.restype = ctypes.c_int
@@ -99,6 +100,12 @@ def gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_MAJOR, stream=No
 def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_MAJOR, stream=None) -> int:
     """C = A . B with bfloat16 operands and output; raw device pointers."""
     return _call("gemm_bf16", M, N, K, A, lda, B, ldb, C, ldc, layout, stream)
+
+
+def gemm_bf16_static_scratch(M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_MAJOR, stream=None) -> int:
+    """gemm_bf16 without any allocation (scratch from the library's fixed
+    16 MiB device array); raw device pointers. See the C header for limits."""
+    return _call("gemm_bf16_static_scratch", M, N, K, A, lda, B, ldb, C, ldc, layout, stream)
 
 
 _BY_DTYPE = {torch.float32: "gemm_tf32", torch.float16: "gemm_f16", torch.bfloat16: "gemm_bf16"}

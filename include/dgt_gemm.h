@@ -79,6 +79,7 @@ extern "C" {
 #define GEMM_ERR_NOT_DEVICE_MEMORY 5  /* a pointer is not device or managed memory of the current device */
 #define GEMM_ERR_DRIVER 6             /* the driver's tensor-map encoder is missing or rejected a map */
 #define GEMM_ERR_DEVICE_TIMEOUT 7     /* returned by gemm_get_device_status when a kernel gave up waiting */
+#define GEMM_ERR_SCRATCH_LIMIT 8      /* gemm_bf16_static_scratch: the shape needs more than its fixed scratch */
 
 /* Limits: M, N, K < 2^31; the number of 128 x 128 output tiles < 2^31. */
 
@@ -93,6 +94,34 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, co
 /* C = A . B with bfloat16 inputs and output (uint16_t bit patterns). */
 int gemm_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
               uint16_t* C, int64_t ldc, int layout, void* stream);
+
+/*
+ * gemm_bf16_static_scratch: gemm_bf16 for callers that cannot allocate.
+ * (The GEMM pages have no counterpart to this call.)
+ *
+ * Same arguments, arithmetic and results as gemm_bf16, but no memory is ever
+ * allocated: where gemm_bf16 allocates a scratch buffer per stream (the first
+ * time a shape splits its last round of tiles along K), this call uses a fixed
+ * array inside the library's device image instead -- for a serving process
+ * whose memory pool already owns the device, a plug-in that must not allocate
+ * behind its host application, or a latency-bound path that cannot take the
+ * synchronisation a cudaFree implies.
+ *
+ * Limit: the array holds 16 MiB of fp32 partial tiles (64 split work items of
+ * 256 KiB, plus their counters). A shape whose plan needs more is refused with
+ * GEMM_ERR_SCRATCH_LIMIT and nothing is launched; shapes that split nothing
+ * use no scratch at all. Every GPU that loads the library keeps the array
+ * (16 MiB + 16 KiB) until the process exits.
+ *
+ * The first call on each device, with that device current, looks up the
+ * array's device address and zeroes its counters (a short synchronous step);
+ * make that first call before any stream capture. Every call shares the one
+ * array: calls that overlap on the GPU (different streams, no ordering between
+ * them) race on it and may produce wrong results; calls ordered on one stream
+ * are safe, since each call's counters are tagged with that call.
+ */
+int gemm_bf16_static_scratch(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
+                             int64_t ldb, uint16_t* C, int64_t ldc, int layout, void* stream);
 
 /* Static English text for a return code; never NULL. */
 const char* gemm_status_string(int status);

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, 8):
+    for code in range(0, 9):
         s = gemm.status_string(code)
         assert s and s != "unknown status"
     assert gemm.status_string(99) == "unknown status"
