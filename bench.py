@@ -259,13 +259,28 @@ def run_ours(args, world, rank, local):
     return line, rank
 
 
+def _kernel_sources_sha256():
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "dense_gemm_tensor_gb300", "csrc")
+    paths = sorted(glob.glob(os.path.join(csrc, "*.cu*")) + glob.glob(os.path.join(csrc, "*.h")))
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _traffic_record(dtype):
-    """DRAM bytes per launch from the committed ncu summary of the current kernel, if any."""
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) from the
+    committed summary, or None when the kernel sources changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
+    if d.get("kernel_sources_sha256") != _kernel_sources_sha256():
+        return None
     return d.get(dtype)
 
 
