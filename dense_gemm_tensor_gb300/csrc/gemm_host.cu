@@ -19,6 +19,52 @@ namespace dgt {
 // most recently aborted launch. One copy per device that loads the library.
 __device__ uint32_t g_status_words[2];
 
+// Copies a rows x row_bytes matrix from a source whose row starts are only
+// `gran`-byte aligned (gran in {2, 4, 8, 16}) to a destination with 16-byte
+// aligned rows of dst_ld_bytes. Each thread moves one 16-byte destination
+// chunk (consecutive threads take consecutive chunks of a row, so reads and
+// writes coalesce); bytes of the last chunk beyond row_bytes are zero.
+__global__ void __launch_bounds__(256) pack_rows_kernel(const uint8_t* __restrict__ src, long long src_ld_bytes,
+                                                        uint8_t* __restrict__ dst, long long dst_ld_bytes,
+                                                        int rows, long long row_bytes, int gran) {
+  const long long chunks_per_row = (row_bytes + 15) / 16;
+  const long long total = chunks_per_row * rows;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / chunks_per_row;
+    const long long c = i - r * chunks_per_row;
+    const uint8_t* s = src + r * src_ld_bytes + c * 16;
+    const long long valid = row_bytes - c * 16;  // > 0
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (valid >= 16) {
+      if (gran == 16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(s);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+      } else if (gran == 8) {
+        const uint2 a = reinterpret_cast<const uint2*>(s)[0], b = reinterpret_cast<const uint2*>(s)[1];
+        w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
+      } else if (gran == 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = reinterpret_cast<const uint32_t*>(s)[q];
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          w[q] = uint32_t(reinterpret_cast<const uint16_t*>(s)[2 * q]) |
+                 (uint32_t(reinterpret_cast<const uint16_t*>(s)[2 * q + 1]) << 16);
+      }
+    } else {
+      // ragged end of the row: 2-byte pieces (every element size here is a multiple of 2)
+      uint16_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int q = 0; q < 8; ++q)
+        if (2 * q < valid) h[q] = reinterpret_cast<const uint16_t*>(s)[q];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) w[q] = uint32_t(h[2 * q]) | (uint32_t(h[2 * q + 1]) << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + r * dst_ld_bytes + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -165,6 +211,8 @@ int pair_clusters(int dev, int kind, bool kmajor, int bn) {
 // never share it. The counters carry the launch epoch, so they are zeroed once
 // at allocation and never reset between calls.
 constexpr int kMaxTailSegs = 4;
+constexpr int kMinSegmentSlabs = 16;         // k-slabs per segment below which splitting does not pay
+constexpr double kSplitPublishCycles = 4000;  // ~2 us at 2 GHz per segment publish/read of a partial
 constexpr size_t kCounterBytes = kSplitCounterBytes;  // up to 1024 split tiles
 
 size_t workspace_bytes(int split_tiles, int segs, int bn) {
@@ -269,20 +317,36 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
     // into `segs` pieces run by different pairs (fp32 partials summed at the end)
     const int fs = g_force_split.load(std::memory_order_relaxed);
     int segs = 1;
-    if (pair && rest > 0 && fs != 1 && kslabs >= 8) {
+    if (pair && rest > 0 && fs != 1) {
       segs = int(conc / rest);
       if (segs > kMaxTailSegs) segs = kMaxTailSegs;
+      while (segs > 1 && kslabs / segs < kMinSegmentSlabs) --segs;
       if (segs < 1) segs = 1;
     }
     const double tile_cost = double(kslabs) * slab_cycles(bn, cols) + 600.0;
     double cost = double(full) * tile_cost;
-    if (rest > 0) cost += segs > 1 ? tile_cost / segs + 1200.0 : tile_cost;
+    if (rest > 0) {
+      // a split tile also publishes a 128 KiB fp32 partial per CTA (~2 us) and its
+      // last segment reads the other segments' partials back (~2 us each)
+      const double split_cost = tile_cost / segs + kSplitPublishCycles * segs;
+      if (segs > 1 && split_cost >= tile_cost) segs = 1;
+      cost += segs > 1 ? split_cost : tile_cost;
+    }
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       const int64_t tiles_m = (M + rows - 1) / rows;
       const int64_t work = tiles + (segs - 1) * rest;
       const int64_t grid_tiles = work < conc ? work : conc;
-      const int band = pair ? 2 : 8;  // measured best at 4096^3: 1-4 pair rows, 4-8 single-CTA rows
+      // band height: 2 pair rows / 8 single-CTA rows (measured best at 4096^3) while
+      // B stays resident in L2; for a larger B, which is re-read once per band,
+      // as many rows as keep the band's A rows within ~40 MB of L2
+      const int band_min = pair ? 2 : 8;
+      int band = band_min;
+      if (double(K) * double(N) * es > 64.0e6) {
+        band = int(40.0e6 / (double(rows) * double(K) * es));
+        if (band < band_min) band = band_min;
+        if (band > 16) band = 16;
+      }
       best = TilePlan{pair, bn, int(tiles_m < band ? tiles_m : band), int(pair ? 2 * grid_tiles : grid_tiles),
                       segs, conc};
     }
@@ -344,11 +408,45 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   LaunchPlan L;
   memset(&L, 0, sizeof(L));
   GemmParams& p = L.p;
-  const int ga = granularity(A, lda, es), gb = granularity(B, ldb, es);
+  int ga = granularity(A, lda, es), gb = granularity(B, ldb, es);
   const bool kmajor = layout == GEMM_B_K_MAJOR;
   int dev_id = 0;
   cudaGetDevice(&dev_id);
-  const TilePlan plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, ga == 16 && gb == 16, dev->sm_count);
+  // Operands whose rows TMA cannot address are packed into 16-byte-aligned
+  // rows in the stream's scratch first (a bandwidth-bound copy), so that the
+  // TMA kernels run; without scratch the kernel's copy warps read them in place.
+  const bool may_pack = ext == nullptr && !(g_debug_flags.load(std::memory_order_relaxed) & DEBUG_NO_PACK);
+  const bool pack_a = may_pack && ga < 16, pack_b = may_pack && gb < 16;
+  TilePlan plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, (ga == 16 || pack_a) && (gb == 16 || pack_b),
+                              dev->sm_count);
+  // Scratch for this plan, laid out as [counters][split partials][packed A][packed B].
+  const int64_t lda_p = pack_a ? (K + 16 / es - 1) / (16 / es) * (16 / es) : lda;
+  const int64_t b_rows = kmajor ? N : K, b_cols = kmajor ? K : N;
+  const int64_t ldb_p = pack_b ? (b_cols + 16 / es - 1) / (16 / es) * (16 / es) : ldb;
+  auto split_tiles = [&](const TilePlan& pl) {
+    const int64_t tm = (M + (pl.pair ? 255 : 127)) / (pl.pair ? 256 : 128), tn = (N + pl.bn - 1) / pl.bn;
+    const int64_t r = (pl.pair && pl.segs > 1) ? (tm * tn) % pl.conc : 0;
+    return (r > 0 && r <= 1024) ? int(r) : 0;
+  };
+  int rest = split_tiles(plan);
+  size_t split_bytes = rest ? workspace_bytes(rest, plan.segs, plan.bn) : 0;
+  const size_t off_a = (split_bytes + 255) / 256 * 256;
+  const size_t off_b = off_a + (pack_a ? (size_t(M) * size_t(lda_p) * es + 255) / 256 * 256 : 0);
+  const size_t total = off_b + (pack_b ? size_t(b_rows) * size_t(ldb_p) * es : 0);
+  char* ws = nullptr;
+  if (ext != nullptr) {
+    if (rest) {
+      if (split_bytes > ext->bytes) return GEMM_ERR_SCRATCH_LIMIT;
+      ws = static_cast<char*>(ext->ptr);
+    }
+  } else if (total > 0) {
+    ws = static_cast<char*>(stream_workspace(dev_id, stream, total < kCounterBytes ? kCounterBytes : total));
+    if (ws == nullptr) {
+      // no scratch: no split tail, and unaligned operands are read in place by the copy warps
+      if (pack_a || pack_b) plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, ga == 16 && gb == 16, dev->sm_count);
+      rest = 0;
+    }
+  }
   const int bn = plan.bn;
   const int64_t tiles_m = (M + (plan.pair ? 255 : 127)) / (plan.pair ? 256 : 128);
   const int64_t tiles_n = (N + bn - 1) / bn;
@@ -363,25 +461,29 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   p.tail_start = p.num_tiles;
   p.tail_segs = 1;
   p.num_work = p.num_tiles;
-  if (plan.pair && plan.segs > 1) {
-    // the last partial round of pair tiles: each tile becomes `segs` k-slab segments
-    const int rest = p.num_tiles % plan.conc;
-    const size_t need = workspace_bytes(rest, plan.segs, bn);
-    void* ws = nullptr;
-    if (ext != nullptr) {
-      if (rest > 1024 || need > ext->bytes) return GEMM_ERR_SCRATCH_LIMIT;
-      ws = ext->ptr;
-    } else if (rest > 0 && rest <= 1024) {
-      ws = stream_workspace(dev_id, stream, need);
-    }
-    if (ws != nullptr) {
-      p.tail_segs = plan.segs;
-      p.tail_start = p.num_tiles - rest;
-      p.num_work = p.tail_start + rest * plan.segs;
-      p.ws_ctr = static_cast<unsigned long long*>(ws);
-      p.ws = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
-    }
+  if (ws != nullptr && rest > 0) {
+    p.tail_segs = plan.segs;
+    p.tail_start = p.num_tiles - rest;
+    p.num_work = p.tail_start + rest * plan.segs;
+    p.ws_ctr = reinterpret_cast<unsigned long long*>(ws);
+    p.ws = reinterpret_cast<float*>(ws + kCounterBytes);
   }
+  if (pack_a && ws != nullptr) {
+    if (launch_pack(A, lda * es, ws + off_a, lda_p * es, M, K * es, ga, stream, dev->sm_count) != cudaSuccess)
+      return GEMM_ERR_LAUNCH;
+    A = ws + off_a;
+    lda = lda_p;
+    ga = 16;
+  }
+  if (pack_b && ws != nullptr) {
+    if (launch_pack(B, ldb * es, ws + off_b, ldb_p * es, b_rows, b_cols * es, gb, stream, dev->sm_count) !=
+        cudaSuccess)
+      return GEMM_ERR_LAUNCH;
+    B = ws + off_b;
+    ldb = ldb_p;
+    gb = 16;
+  }
+  if (plan.pair && !(ga == 16 && gb == 16)) return GEMM_ERR_LAUNCH;  // the pair kernel needs TMA operands
   p.A = A;
   p.lda = lda;
   p.B = B;
@@ -393,7 +495,8 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   p.copy_bytes = 16;
   if (!p.a_tma) p.copy_bytes = ga;
   if (!p.b_tma && gb < p.copy_bytes) p.copy_bytes = gb;
-  p.c_vec = granularity(C, ldc, es) == 16;
+  p.c_gran = granularity(C, ldc, es);
+  p.c_vec = p.c_gran == 16;
   p.status = dev->status_words;
   uint32_t ep = g_epoch.fetch_add(1, std::memory_order_relaxed);
   if (ep == 0) ep = g_epoch.fetch_add(1, std::memory_order_relaxed);
@@ -439,6 +542,19 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
 }
 
 }  // namespace
+
+cudaError_t launch_pack(const void* src, int64_t src_ld_bytes, void* dst, int64_t dst_ld_bytes, int64_t rows,
+                        int64_t row_bytes, int gran, cudaStream_t stream, int sm_count) {
+  const long long chunks = (row_bytes + 15) / 16 * rows;
+  long long blocks = (chunks + 255) / 256;
+  if (blocks > 8LL * sm_count) blocks = 8LL * sm_count;
+  pack_rows_kernel<<<int(blocks), 256, 0, stream>>>(static_cast<const uint8_t*>(src), src_ld_bytes,
+                                                    static_cast<uint8_t*>(dst), dst_ld_bytes, int(rows), row_bytes,
+                                                    gran);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
 
 int run_gemm_external(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                       int64_t ldb, void* C, int64_t ldc, int layout, void* stream, const ExternalScratch* ext) {

@@ -73,7 +73,10 @@ enum : uint32_t {
   ROLE_COPY = 4u << 4,
   ROLE_TEARDOWN = 5u << 4,
 };
-enum : uint32_t { DEBUG_STALL_PRODUCER = 1u };
+enum : uint32_t {
+  DEBUG_STALL_PRODUCER = 1u,
+  DEBUG_NO_PACK = 2u,  // host: copy unaligned operands with the kernel's copy warps instead of packing them
+};
 
 struct GemmParams {
   int M, N, K;
@@ -96,6 +99,7 @@ struct GemmParams {
   int a_tma, b_tma;  // operand loaded by TMA (1) or by the copy warps (0)
   int copy_bytes;    // copy-warp granularity in bytes: 16, 8, 4 or 2
   int c_vec;         // C base and row pitch allow 16-byte stores
+  int c_gran;        // widest store (bytes: 16, 8, 4 or 2) the C base and row pitch allow
   uint32_t* status;  // device status words [2]
   uint32_t epoch;    // unique per launch
   uint32_t debug;
@@ -321,6 +325,25 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, in
         dst[q] = make_uint4(pack2<KIND>(r[8 * q], r[8 * q + 1]), pack2<KIND>(r[8 * q + 2], r[8 * q + 3]),
                             pack2<KIND>(r[8 * q + 4], r[8 * q + 5]), pack2<KIND>(r[8 * q + 6], r[8 * q + 7]));
     }
+  } else if (p.c_gran >= 4 && col0 + 32 <= p.N) {
+    // unaligned rows: the widest stores the row start allows (4 or 8 bytes)
+    uint32_t w[KIND == KIND_TF32 ? 32 : 16];
+    if constexpr (KIND == KIND_TF32) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w[j] = r[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = pack2<KIND>(r[2 * j], r[2 * j + 1]);
+    }
+    constexpr int NW = KIND == KIND_TF32 ? 32 : 16;
+    uint8_t* dst = reinterpret_cast<uint8_t*>(p.C) + idx0 * (KIND == KIND_TF32 ? 4 : 2);
+    if (p.c_gran >= 8) {
+#pragma unroll
+      for (int j = 0; j < NW / 2; ++j) reinterpret_cast<uint2*>(dst)[j] = make_uint2(w[2 * j], w[2 * j + 1]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < NW; ++j) reinterpret_cast<uint32_t*>(dst)[j] = w[j];
+    }
   } else {
     const int lim = min(32, p.N - col0);
 #pragma unroll
@@ -328,6 +351,7 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, in
       if (j < lim) store_one<KIND>(p.C, idx0 + j, r[j]);
   }
 }
+
 
 // Reads `nchunks` 32-column chunks of this warp's 32 accumulator rows from
 // tensor memory and hands each to `use(c, r)`, keeping the next chunk's load

@@ -109,15 +109,18 @@ def gemm_bf16_static_scratch(M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_
 
 
 _BY_DTYPE = {torch.float32: "gemm_tf32", torch.float16: "gemm_f16", torch.bfloat16: "gemm_bf16"}
+_FN = {}  # dtype -> bound C function, filled on first use
 
 
 def _rows(t: torch.Tensor, what: str) -> int:
     """Leading dimension of a 2-D tensor with unit column stride."""
     if t.dim() != 2:
         raise ValueError(f"{what} must be 2-D")
-    if t.shape[1] > 1 and t.stride(1) != 1:
+    rows, cols = t.shape
+    s0, s1 = t.stride()
+    if cols > 1 and s1 != 1:
         raise ValueError(f"{what} must have unit stride along its rows")
-    return max(t.stride(0), t.shape[1]) if t.shape[0] > 1 else t.shape[1]
+    return (s0 if s0 > cols else cols) if rows > 1 else cols
 
 
 def matmul(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, layout: int = GEMM_B_ROW_MAJOR,
@@ -130,8 +133,14 @@ def matmul(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *,
     the entry point: float32 -> gemm_tf32, float16 -> gemm_f16, bfloat16 ->
     gemm_bf16. ``out`` (M x N, same dtype) may have padded rows too.
     """
-    if A.dtype not in _BY_DTYPE or B.dtype != A.dtype:
-        raise TypeError("A and B must both be float32, float16 or bfloat16")
+    dt = A.dtype
+    fn = _FN.get(dt)
+    if fn is None:
+        if dt not in _BY_DTYPE:
+            raise TypeError("A and B must both be float32, float16 or bfloat16")
+        fn = _FN[dt] = getattr(load(), _BY_DTYPE[dt])
+    if B.dtype != dt:
+        raise TypeError("A and B must have the same dtype")
     if not (A.is_cuda and B.is_cuda):
         raise ValueError("A and B must be CUDA tensors")
     M, K = A.shape
@@ -144,14 +153,14 @@ def matmul(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *,
             raise ValueError("B must be N x K for the K-major layout")
         N = B.shape[0]
     if out is None:
-        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
-    elif out.shape != (M, N) or out.dtype != A.dtype:
+        out = torch.empty((M, N), dtype=dt, device=A.device)
+    elif out.dtype != dt or tuple(out.shape) != (M, N):
         raise ValueError("out must be M x N with the operands' dtype")
-    s = stream if stream is not None else torch.cuda.current_stream(A.device)
-    code = _call(_BY_DTYPE[A.dtype], M, N, K, A.data_ptr() or None, _rows(A, "A"), B.data_ptr() or None,
-                 _rows(B, "B"), out.data_ptr() or None, _rows(out, "out"), layout, s.cuda_stream)
+    s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    code = fn(M, N, K, A.data_ptr() or None, _rows(A, "A"), B.data_ptr() or None, _rows(B, "B"),
+              out.data_ptr() or None, _rows(out, "out"), layout, s)
     if code != GEMM_OK:
-        raise GemmError(code, _BY_DTYPE[A.dtype])
+        raise GemmError(code, _BY_DTYPE[dt])
     return out
 
 

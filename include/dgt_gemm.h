@@ -54,8 +54,10 @@
  *
  * Any base address and leading dimension that keeps elements aligned to
  * their size is accepted. Rows whose byte pitch is a multiple of 16 (and 16-byte
- * aligned bases) are streamed with TMA; other operands are copied by the
- * kernel's own copy warps, which is slower but gives the same results.
+ * aligned bases) are streamed with TMA; another A or B is first packed into
+ * 16-byte-aligned rows in the stream's scratch buffer (one bandwidth-bound
+ * copy kernel), and if no scratch can be had it is read in place by the
+ * kernel's copy warps, which is slower but gives the same results.
  */
 #ifndef DGT_GEMM_H
 #define DGT_GEMM_H
@@ -144,7 +146,9 @@ int gemm_reset_device_status(void);
  * Test hooks, process-wide, for subsequent calls. `wait_limit_ns` bounds every
  * wait inside the kernels (0 keeps the default of 1 s). Flag bit 0 makes the
  * TMA producer issue nothing, so the MMA issuer's first wait runs out: the
- * kernel records a timeout and returns with C unspecified. Pass 0, 0 to restore.
+ * kernel records a timeout and returns with C unspecified. Flag bit 1 reads
+ * operands whose rows TMA cannot address in place with the kernel's copy warps
+ * instead of packing them into aligned scratch first. Pass 0, 0 to restore.
  */
 int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns);
 

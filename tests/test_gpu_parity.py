@@ -135,11 +135,12 @@ def test_pair_kernel_full(dtype, layout, tile_n):
 
 @pytest.mark.parametrize("dtype", ["bf16", "tf32"])
 @pytest.mark.parametrize("layout", [0, 1])
-@pytest.mark.parametrize("shape", [(768, 2560, 1000), (1280, 1024, 1000), (768, 1024, 1000), (4096, 4096, 512)])
+@pytest.mark.parametrize("shape", [(768, 2560, 4096), (1280, 1024, 4096), (768, 1024, 4096), (4096, 4096, 512)])
 def test_pair_split_tail(dtype, layout, shape):
     """Tiles of the last partial round split along K (2-4 segments, chosen
-    from the co-resident pair count): full parity, and bitwise-equal results
-    over repeated runs whatever segment arrives last."""
+    from the co-resident pair count when each segment keeps >= 16 k-slabs):
+    full parity, and bitwise-equal results over repeated runs whatever segment
+    arrives last."""
     M, N, K = shape
     gemm.set_tuning(2, 256, 0, 0)
     try:
@@ -148,7 +149,7 @@ def test_pair_split_tail(dtype, layout, shape):
         plan = gemm.last_plan()
         assert plan["kernel"] == 2
         tiles = -(-M // 256) * -(-N // 256)
-        if tiles % plan["concurrent_tiles"]:
+        if K == 4096 and tiles % plan["concurrent_tiles"]:
             assert plan["tail_segs"] > 1, plan
         assert plan["work_items"] == plan["tail_start"] + (tiles - plan["tail_start"]) * plan["tail_segs"]
         _check_full(p, C1)
@@ -184,13 +185,19 @@ def test_small_integers_bit_exact(dtype, layout):
     ("tf32", 202, 522, 520),   # 8-byte granularity, aligned C
 ])
 @pytest.mark.parametrize("layout", [0, 1])
-def test_unaligned_pitches_full(dtype, lda, ldb, ldc, layout):
-    """Row pitches TMA cannot address go through the copy warps."""
+@pytest.mark.parametrize("pack", [True, False])
+def test_unaligned_pitches_full(dtype, lda, ldb, ldc, layout, pack):
+    """Row pitches TMA cannot address: packed into aligned scratch first (the
+    default), or read in place by the kernel's copy warps (test hook)."""
     M, N, K = 300, 520, 200
     if layout == 1:
         ldb = lda + 3
     p = inputs.make_problem("unal", dtype, M, N, K, lda=lda, ldb=ldb, layout=layout, seed_a=5, seed_b=6)
-    C, Cbuf = _run(p, ldc=ldc, fill=7.0)
+    gemm.set_debug(0 if pack else 2, 0)
+    try:
+        C, Cbuf = _run(p, ldc=ldc, fill=7.0)
+    finally:
+        gemm.set_debug(0, 0)
     _check_full(p, C)
     assert torch.all(Cbuf[:, N:] == 7.0)
 
@@ -268,7 +275,10 @@ def test_workload_full(name):
     p = inputs.workload(name)
     C, _ = _run(p)
     res = _check_full(p, C)
-    print(name, res)
+    print(name, res, gemm.last_plan())
+    if name == "bf16_ragged":
+        # 8200-byte rows of B and C: B is packed, so the TMA pair kernel runs
+        assert gemm.last_plan()["kernel"] == 2
 
 
 @pytest.mark.parametrize("name", ["bf16_8192", "bf16_16384", "bf16_proj"])

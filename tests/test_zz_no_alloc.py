@@ -45,7 +45,7 @@ def _pointers(p):
     return A, B
 
 
-@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (768, 2560, 1000), (300, 520, 200)])
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (768, 2560, 4096), (300, 520, 200)])
 def test_matches_gemm_bf16_on_two_calls(shape):
     M, N, K = shape
     p = inputs.make_problem("noalloc", "bf16", M, N, K, dist_a="normal", dist_b="normal", seed_a=M + 3, seed_b=N + 5)
@@ -74,8 +74,8 @@ def test_split_shape_uses_the_fixed_scratch_and_big_needs_are_refused():
     """A shape whose last round splits runs inside the 16 MiB; a plan needing
     more is refused with GEMM_ERR_SCRATCH_LIMIT and launches nothing."""
     # 1536 x 4864: 114 tiles of 256 x 256; with 76 co-resident pairs the last
-    # round's 38 tiles split in two -> 76 items of 256 KiB = 19 MiB
-    M, N, K = 1536, 4864, 1024
+    # round's 38 tiles split in two along K -> 76 items of 256 KiB = 19 MiB
+    M, N, K = 1536, 4864, 4096
     p = inputs.make_problem("noalloc_big", "bf16", M, N, K, seed_a=11, seed_b=12)
     A, B = _pointers(p)
     ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
