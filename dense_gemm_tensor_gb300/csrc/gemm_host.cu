@@ -182,7 +182,7 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 }
 
 // Co-resident CTA pairs of each pair-kernel variant, per device (-1 = not queried yet).
-std::atomic<int> g_pair_clusters[kMaxDevices][3][2][2];
+std::atomic<int> g_pair_clusters[kMaxDevices][3][2][4];
 std::once_flag g_pair_once;
 
 int pair_clusters(int dev, int kind, bool kmajor, int bn) {
@@ -192,7 +192,8 @@ int pair_clusters(int dev, int kind, bool kmajor, int bn) {
         for (auto& c : b)
           for (auto& d : c) d.store(-1);
   });
-  std::atomic<int>& slot = g_pair_clusters[dev][kind][kmajor ? 1 : 0][bn == 256 ? 0 : 1];
+  const int wi = bn == 256 ? 0 : bn == 224 ? 1 : bn == 192 ? 2 : 3;
+  std::atomic<int>& slot = g_pair_clusters[dev][kind][kmajor ? 1 : 0][wi];
   int n = slot.load(std::memory_order_acquire);
   if (n < 0) {
     n = kind == KIND_TF32 ? pair_clusters_tf32(kmajor, bn)
@@ -213,6 +214,7 @@ int pair_clusters(int dev, int kind, bool kmajor, int bn) {
 constexpr int kMaxTailSegs = 4;
 constexpr int kMinSegmentSlabs = 16;         // k-slabs per segment below which splitting does not pay
 constexpr double kSplitPublishCycles = 4000;  // ~2 us at 2 GHz per segment publish/read of a partial
+constexpr double kPairLaunchCycles = 8000;    // extra fixed cost of the pair kernel's launch and set-up
 constexpr size_t kCounterBytes = kSplitCounterBytes;  // up to 1024 split tiles
 
 size_t workspace_bytes(int split_tiles, int segs, int bn) {
@@ -298,8 +300,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
     int cols;  // B columns one SM loads per slab
     if (pair) {
       if (!all_tma) return;
-      if (!kmajor && (bn / 2) % atom != 0) return;
-      cols = bn / 2;
+      cols = kmajor ? bn / 2 : (bn / 2 + atom - 1) / atom * atom;
     } else {
       cols = kmajor ? bn : (bn + atom - 1) / atom * atom;
     }
@@ -324,7 +325,8 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
       if (segs < 1) segs = 1;
     }
     const double tile_cost = double(kslabs) * slab_cycles(bn, cols) + 600.0;
-    double cost = double(full) * tile_cost;
+    // a cluster launch with pair set-up costs ~4 us more than a plain one (measured)
+    double cost = double(full) * tile_cost + (pair ? kPairLaunchCycles : 0.0);
     if (rest > 0) {
       // a split tile also publishes a 128 KiB fp32 partial per CTA (~2 us) and its
       // last segment reads the other segments' partials back (~2 us each)

@@ -43,7 +43,7 @@ struct PairCfg {
   static constexpr int KSTEPS = BK / UK;
   static constexpr int A_BYTES = BM * 128;
   static constexpr int BOXN = 128 / ES;
-  static constexpr int NBOX = BNH / BOXN;
+  static constexpr int NBOX = (BNH + BOXN - 1) / BOXN;  // MN-major B: boxes per CTA (last may be partly used)
   static constexpr int BOX_BYTES = BK * 128;
   static constexpr int B_BYTES = B_KMAJOR ? BNH * 128 : NBOX * BOX_BYTES;
   static constexpr bool B_ATOM32 = (ES == 4) && !B_KMAJOR;
@@ -60,8 +60,8 @@ struct PairCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + RESERVED;
   static constexpr int PARTIAL_FLOATS = BM * BN;  // one CTA's fp32 partial tile
-  static_assert(B_KMAJOR || NBOX * BOXN == BNH, "MN-major B: each CTA's half must be whole 128-byte slabs");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
+  static_assert(BNH % 16 == 0, "each CTA's B half is whole 16-column groups");
   static_assert(ACC_BUFS * BN <= 512, "tensor memory");
   static_assert(NUM_BARS * 8 + 32 <= 256, "barrier area");
   static_assert(STAGES >= 3, "pipeline depth");
@@ -173,7 +173,9 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 4) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
-    if (lane == 0 && !(p.debug & DEBUG_STALL_PRODUCER)) {
+    // The whole warp walks the loop (so addresses and coordinates stay
+    // warp-uniform); one elected lane issues.
+    if (!(p.debug & DEBUG_STALL_PRODUCER)) {
       int it = 0;
       bool ok = true;
       for (int w = pair; ok && w < p.num_work; w += npairs) {
@@ -183,69 +185,85 @@ __global__ void __launch_bounds__(192, 1)
         for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!wait_phase(p, empty0 + 8 * s, ph ^ 1, ROLE_PRODUCER | (s << 8))) {
+          if (!warp_wait_phase(p, empty0 + 8 * s, ph ^ 1, ROLE_PRODUCER | (s << 8))) {
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_BYTES);
           const uint32_t fb = mapa_shared(full0 + 8 * s, 0);
-          tma_load_2d_pair(sA + s * Cf::A_BYTES, &tmA, fb, kb * Cf::BK, row0);
-          if constexpr (B_KMAJOR) {
-            tma_load_2d_pair(sB + s * Cf::B_BYTES, &tmB, fb, kb * Cf::BK, col0);
-          } else {
+          const uint32_t a_dst = sA + s * Cf::A_BYTES;
+          const uint32_t b_dst = sB + s * Cf::B_BYTES;
+          if (elect_one()) {
+            if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_BYTES);
+            tma_load_2d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0);
+            if constexpr (B_KMAJOR) {
+              tma_load_2d_pair(b_dst, &tmB, fb, kb * Cf::BK, col0);
+            } else {
 #pragma unroll
-            for (int j = 0; j < Cf::NBOX; ++j)
-              tma_load_2d_pair(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, col0 + j * Cf::BOXN,
-                               kb * Cf::BK);
+              for (int j = 0; j < Cf::NBOX; ++j)
+                tma_load_2d_pair(b_dst + j * Cf::BOX_BYTES, &tmB, fb, col0 + j * Cf::BOXN, kb * Cf::BK);
+            }
           }
+          __syncwarp();
         }
       }
-      *issued_slot = it;
+      if (lane == 0) *issued_slot = it;
     }
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer (leader only)
-    if (leader && lane == 0) {
+    // The whole warp walks the loop and builds the descriptors (warp-uniform);
+    // one elected lane -- the same lane every time -- issues the MMAs and commits.
+    if (leader) {
       int it = 0, tc = 0;
       bool ok = true;
       for (int w = pair; ok && w < p.num_work; w += npairs, ++tc) {
         const PairWork wk = pair_work(p, w);
         const int b = tc % NB;
         const uint32_t use = (tc / NB) & 1;
-        if (!wait_phase(p, acce0 + 8 * b, use ^ 1, ROLE_MMA | (0x80u << 8))) break;
+        if (!warp_wait_phase(p, acce0 + 8 * b, use ^ 1, ROLE_MMA | (0x80u << 8))) break;
         tc_fence_after();
         const uint32_t d = tmem + b * Cf::ACC_COLS;
         for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!wait_phase(p, full0 + 8 * s, ph, ROLE_MMA | (s << 8))) {
+          if (!warp_wait_phase(p, full0 + 8 * s, ph, ROLE_MMA | (s << 8))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_addr = sA + s * Cf::A_BYTES;
           const uint32_t b_addr = sB + s * Cf::B_BYTES;
+          uint64_t ad[Cf::KSTEPS], bd[Cf::KSTEPS];
 #pragma unroll
           for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
-            const uint64_t ad = sdesc(a_addr + kk * 32, 16, 1024, SWZ_128B);
-            uint64_t bd;
+            ad[kk] = sdesc(a_addr + kk * 32, 16, 1024, SWZ_128B);
             if constexpr (B_KMAJOR)
-              bd = sdesc(b_addr + kk * 32, 16, 1024, SWZ_128B);
+              bd[kk] = sdesc(b_addr + kk * 32, 16, 1024, SWZ_128B);
             else
-              bd = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
-            const uint32_t acc = (kb > wk.kb0 || kk > 0) ? 1u : 0u;
-            if constexpr (KIND == KIND_TF32)
-              mma_tf32_pair(d, ad, bd, Cf::IDESC, acc);
-            else
-              mma_f16_pair(d, ad, bd, Cf::IDESC, acc);
+              bd[kk] = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
           }
-          mma_commit_pair(empty0 + 8 * s, 0x3);  // both CTAs may refill stage s
+          const uint32_t first = (kb == wk.kb0) ? 0u : 1u;
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
+              const uint32_t acc = kk > 0 ? 1u : first;
+              if constexpr (KIND == KIND_TF32)
+                mma_tf32_pair(d, ad[kk], bd[kk], Cf::IDESC, acc);
+              else
+                mma_f16_pair(d, ad[kk], bd[kk], Cf::IDESC, acc);
+            }
+            mma_commit_pair(empty0 + 8 * s, 0x3);  // both CTAs may refill stage s
+          }
+          __syncwarp();
         }
         if (!ok) break;
-        mma_commit_pair(accf0 + 8 * b, 0x3);  // both halves of the accumulator ready
+        if (elect_one()) mma_commit_pair(accf0 + 8 * b, 0x3);  // both halves of the accumulator ready
+        __syncwarp();
       }
-      *consumed_slot = it;
-      mma_commit_pair(drain_bar, 0x1);
-      wait_phase_drain(p, drain_bar, 0);
+      if (lane == 0) *consumed_slot = it;
+      if (elect_one()) mma_commit_pair(drain_bar, 0x1);
+      __syncwarp();
+      if (lane == 0) wait_phase_drain(p, drain_bar, 0);
+      __syncwarp();
     }
   } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue (both CTAs)

@@ -51,7 +51,7 @@ int run_gemm_external(int kind, int64_t M, int64_t N, int64_t K, const void* A, 
 
 // Tile widths the kernels are built for (the host picks one per call).
 constexpr int kTileWidths[] = {256, 224, 192, 128};
-constexpr int kPairTileWidths[] = {256, 128};
+constexpr int kPairTileWidths[] = {256, 224, 192, 128};
 
 
 // Sets the kernel's dynamic shared-memory limit once per device, then launches.
@@ -146,15 +146,27 @@ template <int KIND, bool KMAJ>
 cudaError_t launch_pair_layout(const LaunchPlan& L) {
   switch (L.bn) {
     case 256: return launch_pair_variant<KIND, KMAJ, 256>(L);
+    case 224: return launch_pair_variant<KIND, KMAJ, 224>(L);
+    case 192: return launch_pair_variant<KIND, KMAJ, 192>(L);
     case 128: return launch_pair_variant<KIND, KMAJ, 128>(L);
     default: return cudaErrorInvalidValue;
   }
 }
 
+template <int KIND, bool KMAJ>
+int pair_clusters_layout(int bn) {
+  switch (bn) {
+    case 256: return pair_clusters_variant<KIND, KMAJ, 256>();
+    case 224: return pair_clusters_variant<KIND, KMAJ, 224>();
+    case 192: return pair_clusters_variant<KIND, KMAJ, 192>();
+    case 128: return pair_clusters_variant<KIND, KMAJ, 128>();
+    default: return 0;
+  }
+}
+
 template <int KIND>
 int pair_clusters_kind(bool kmajor, int bn) {
-  if (kmajor) return bn == 256 ? pair_clusters_variant<KIND, true, 256>() : pair_clusters_variant<KIND, true, 128>();
-  return bn == 256 ? pair_clusters_variant<KIND, false, 256>() : pair_clusters_variant<KIND, false, 128>();
+  return kmajor ? pair_clusters_layout<KIND, true>(bn) : pair_clusters_layout<KIND, false>(bn);
 }
 
 template <int KIND>

@@ -172,7 +172,7 @@ int gemm_last_plan(int32_t* out);
  * call, 1 = single-CTA kernel (128-row tiles), 2 = CTA-pair kernel (256-row
  * tiles; only when A and B rows are 16-byte aligned, else the single-CTA
  * kernel runs). `tile_n`: output tile width, 256, 224, 192 or 128 for the
- * single-CTA kernel and 256 or 128 for the pair (0 = chosen per call).
+ * single-CTA kernel and 256, 224, 192 or 128 for the pair (0 = chosen per call).
  * `raster`: band height of the tile order in tile rows (0 = chosen per call).
  * `tail_split`: 0 or 2 = split the tiles of the last partial round along K
  * where the shape allows (the default), 1 = never split.

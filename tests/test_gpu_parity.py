@@ -113,7 +113,7 @@ def test_every_tile_width_full(dtype, layout, tile_n):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
 @pytest.mark.parametrize("layout", [0, 1])
-@pytest.mark.parametrize("tile_n", [256, 128])
+@pytest.mark.parametrize("tile_n", [256, 224, 192, 128])
 def test_pair_kernel_full(dtype, layout, tile_n):
     """The CTA-pair kernel (256-row tiles over two SMs), forced, on shapes
     with a ragged pair-row (M = 129: the second CTA's rows are all past M),
