@@ -2,5 +2,5 @@
 #include "launch.h"
 namespace dgt {
 cudaError_t launch_bf16(const LaunchPlan& L) { return launch_kind<KIND_BF16>(L); }
-int pair_clusters_bf16(bool kmajor, int bn) { return pair_clusters_kind<KIND_BF16>(kmajor, bn); }
+int pair_clusters_bf16(bool kmajor, int bn, int pairs) { return pair_clusters_kind<KIND_BF16>(kmajor, bn, pairs); }
 }  // namespace dgt

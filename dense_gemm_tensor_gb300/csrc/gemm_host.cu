@@ -182,23 +182,24 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 }
 
 // Co-resident CTA pairs of each pair-kernel variant, per device (-1 = not queried yet).
-std::atomic<int> g_pair_clusters[kMaxDevices][3][2][4];
+std::atomic<int> g_pair_clusters[kMaxDevices][3][2][4][2];
 std::once_flag g_pair_once;
 
-int pair_clusters(int dev, int kind, bool kmajor, int bn) {
+int pair_clusters(int dev, int kind, bool kmajor, int bn, int pairs) {
   std::call_once(g_pair_once, [] {
     for (auto& a : g_pair_clusters)
       for (auto& b : a)
         for (auto& c : b)
-          for (auto& d : c) d.store(-1);
+          for (auto& d : c)
+            for (auto& e : d) e.store(-1);
   });
   const int wi = bn == 256 ? 0 : bn == 224 ? 1 : bn == 192 ? 2 : 3;
-  std::atomic<int>& slot = g_pair_clusters[dev][kind][kmajor ? 1 : 0][wi];
+  std::atomic<int>& slot = g_pair_clusters[dev][kind][kmajor ? 1 : 0][wi][pairs - 1];
   int n = slot.load(std::memory_order_acquire);
   if (n < 0) {
-    n = kind == KIND_TF32 ? pair_clusters_tf32(kmajor, bn)
-        : kind == KIND_BF16 ? pair_clusters_bf16(kmajor, bn)
-                            : pair_clusters_f16(kmajor, bn);
+    n = kind == KIND_TF32 ? pair_clusters_tf32(kmajor, bn, pairs)
+        : kind == KIND_BF16 ? pair_clusters_bf16(kmajor, bn, pairs)
+                            : pair_clusters_f16(kmajor, bn, pairs);
     slot.store(n, std::memory_order_release);
   }
   return n;
@@ -217,8 +218,9 @@ constexpr double kSplitPublishCycles = 4000;  // ~2 us at 2 GHz per segment publ
 constexpr double kPairLaunchCycles = 8000;    // extra fixed cost of the pair kernel's launch and set-up
 constexpr size_t kCounterBytes = kSplitCounterBytes;  // up to 1024 split tiles
 
-size_t workspace_bytes(int split_tiles, int segs, int bn) {
-  return kCounterBytes + size_t(split_tiles) * size_t(segs) * 2u * 128u * size_t(bn) * sizeof(float);
+// `ctas`: CTAs per cluster, each publishing its own 128 x bn partial
+size_t workspace_bytes(int split_tiles, int segs, int bn, int ctas) {
+  return kCounterBytes + size_t(split_tiles) * size_t(segs) * size_t(ctas) * 128u * size_t(bn) * sizeof(float);
 }
 
 struct Workspace {
@@ -262,6 +264,7 @@ void free_workspaces() {
 
 struct TilePlan {
   bool pair;
+  int pairs;  // pair kernel: CTA pairs per cluster (2: the pairs share A and take two adjacent tiles)
   int bn;
   int raster;
   int grid;   // CTAs
@@ -269,50 +272,53 @@ struct TilePlan {
   int conc;   // tiles in flight at once (SMs, or co-resident CTA pairs)
 };
 
-// Picks the kernel (single CTA or CTA pair), the tile width and the tile order.
+// Cycles one SM spends per 128-byte k-slab of a tile in the steady state of
+// the k-loop, by kernel (single CTA, CTA pair, two pairs sharing A) and tile
+// width 256/224/192/128, measured on GB300 at 4096^3 (bf16; tf32 takes the
+// same time per slab). The dense MMA rate alone would give 2 x width; the
+// rest is time the MMA issuer waits for operands. Sharing A between two pairs
+// halves the A bytes each SM fetches from L2 but couples four CTAs' pipelines,
+// and measured slower per slab than the pair alone at this size.
+constexpr double kSlabCycles[3][4] = {
+    {672.0, 640.0, 605.0, 570.0},  // single CTA, 128 x width tiles
+    {567.0, 517.0, 498.0, 479.0},  // CTA pair, 256 x width tiles
+    {640.0, 565.0, 560.0, 540.0},  // two pairs sharing A, two 256 x width tiles
+};
+
+// Picks the kernel (single CTA, CTA pair, or two pairs sharing A), the tile
+// width and the tile order.
 //
-// Cost model, per SM and per 128-byte k-slab of a tile: the MMA needs 2 * (tile
-// columns per SM-row block) cycles (128 x BN x one slab at the dense rate), and
-// the SM must receive 16 KB of A plus (B columns it loads) x 128 bytes, at
-// about 68 bytes per cycle (measured on GB300 for this kernel); the slower of
-// the two sets the slab time. A CTA pair computes a 256 x BN tile from half the
-// B bytes per SM. The grid holds one CTA per SM, so a product of T tiles takes
-// ceil(T / concurrent tiles) rounds; the plan with the least total time wins.
-// The band height keeps a band's A rows and the B tiles in flight inside L2.
+// Cost model: a tile takes (k-slabs x kSlabCycles) cycles; the grid holds one
+// CTA per SM, so a product of T work tiles takes ceil(T / concurrent tiles)
+// rounds, the last partial round possibly split along K; the plan with the
+// least total time wins. The band height keeps a band's A rows and the B tiles
+// in flight inside L2.
 TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es, bool kmajor, bool all_tma,
                      int sms) {
-  const int atom = 128 / es;  // MN-major B is fetched in whole 128-byte slabs
   const int64_t kslabs = (K * es + 127) / 128;
   const int fv = g_force_variant.load(std::memory_order_relaxed);
   const int fb = g_force_bn.load(std::memory_order_relaxed);
   const int fr = g_force_raster.load(std::memory_order_relaxed);
-  TilePlan best{false, 256, 8, sms, 1, sms};
+  TilePlan best{false, 1, 256, 8, sms, 1, sms};
   double best_cost = -1.0;
-  auto slab_cycles = [&](int bn, int cols) {
-    const double mma = 2.0 * bn;
-    const double bytes = 128.0 * 128.0 + 128.0 * cols;
-    return mma > bytes / 66.0 ? mma : bytes / 66.0;
-  };
-  auto consider = [&](bool pair, int bn) {
+  auto consider = [&](bool pair, int pairs, int bn) {
     if (fv == 1 && pair) return;
-    if (fv == 2 && !pair) return;
+    if (fv == 2 && !(pair && pairs == 1)) return;
+    if (fv == 3 && !(pair && pairs == 2)) return;
     if (fb && fb != bn) return;
-    int cols;  // B columns one SM loads per slab
+    if (pair && !all_tma) return;
+    int conc;  // work tiles in flight
     if (pair) {
-      if (!all_tma) return;
-      cols = kmajor ? bn / 2 : (bn / 2 + atom - 1) / atom * atom;
-    } else {
-      cols = kmajor ? bn : (bn + atom - 1) / atom * atom;
-    }
-    int conc;  // tiles in flight
-    if (pair) {
-      conc = pair_clusters(dev, kind, kmajor, bn);
+      conc = pair_clusters(dev, kind, kmajor, bn, pairs);
       if (conc <= 0) return;
     } else {
       conc = sms;
     }
+    const int wi = bn == 256 ? 0 : bn == 224 ? 1 : bn == 192 ? 2 : 3;
+    const double slab = kSlabCycles[pair ? pairs : 0][wi];
     const int64_t rows = pair ? 256 : 128;
-    const int64_t tiles = ((M + rows - 1) / rows) * ((N + bn - 1) / bn);
+    const int64_t tiles_n = (N + bn - 1) / bn;
+    const int64_t tiles = ((M + rows - 1) / rows) * ((tiles_n + pairs - 1) / pairs);
     const int64_t full = tiles / conc, rest = tiles % conc;
     // pair kernel: the tiles of the last partial round may be split along K
     // into `segs` pieces run by different pairs (fp32 partials summed at the end)
@@ -324,7 +330,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
       while (segs > 1 && kslabs / segs < kMinSegmentSlabs) --segs;
       if (segs < 1) segs = 1;
     }
-    const double tile_cost = double(kslabs) * slab_cycles(bn, cols) + 600.0;
+    const double tile_cost = double(kslabs) * slab + 600.0;
     // a cluster launch with pair set-up costs ~4 us more than a plain one (measured)
     double cost = double(full) * tile_cost + (pair ? kPairLaunchCycles : 0.0);
     if (rest > 0) {
@@ -349,15 +355,16 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
         if (band < band_min) band = band_min;
         if (band > 16) band = 16;
       }
-      best = TilePlan{pair, bn, int(tiles_m < band ? tiles_m : band), int(pair ? 2 * grid_tiles : grid_tiles),
-                      segs, conc};
+      best = TilePlan{pair, pairs, bn, int(tiles_m < band ? tiles_m : band),
+                      int(pair ? 2 * pairs * grid_tiles : grid_tiles), segs, conc};
     }
   };
-  for (int bn : kPairTileWidths) consider(true, bn);
-  for (int bn : kTileWidths) consider(false, bn);
+  for (int bn : kPairTileWidths) consider(true, 2, bn);
+  for (int bn : kPairTileWidths) consider(true, 1, bn);
+  for (int bn : kTileWidths) consider(false, 1, bn);
   if (best_cost < 0) {  // a forced combination that does not apply: fall back to the single-CTA default
     const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
-    best = TilePlan{false, 256, 8, int(tiles < sms ? tiles : sms), 1, sms};
+    best = TilePlan{false, 1, 256, 8, int(tiles < sms ? tiles : sms), 1, sms};
   }
   if (fr) best.raster = fr;
   return best;
@@ -426,12 +433,13 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   const int64_t b_rows = kmajor ? N : K, b_cols = kmajor ? K : N;
   const int64_t ldb_p = pack_b ? (b_cols + 16 / es - 1) / (16 / es) * (16 / es) : ldb;
   auto split_tiles = [&](const TilePlan& pl) {
-    const int64_t tm = (M + (pl.pair ? 255 : 127)) / (pl.pair ? 256 : 128), tn = (N + pl.bn - 1) / pl.bn;
+    const int64_t tm = (M + (pl.pair ? 255 : 127)) / (pl.pair ? 256 : 128);
+    const int64_t tn = ((N + pl.bn - 1) / pl.bn + pl.pairs - 1) / pl.pairs;
     const int64_t r = (pl.pair && pl.segs > 1) ? (tm * tn) % pl.conc : 0;
     return (r > 0 && r <= 1024) ? int(r) : 0;
   };
   int rest = split_tiles(plan);
-  size_t split_bytes = rest ? workspace_bytes(rest, plan.segs, plan.bn) : 0;
+  size_t split_bytes = rest ? workspace_bytes(rest, plan.segs, plan.bn, 2 * plan.pairs) : 0;
   const size_t off_a = (split_bytes + 255) / 256 * 256;
   const size_t off_b = off_a + (pack_a ? (size_t(M) * size_t(lda_p) * es + 255) / 256 * 256 : 0);
   const size_t total = off_b + (pack_b ? size_t(b_rows) * size_t(ldb_p) * es : 0);
@@ -451,7 +459,9 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   }
   const int bn = plan.bn;
   const int64_t tiles_m = (M + (plan.pair ? 255 : 127)) / (plan.pair ? 256 : 128);
-  const int64_t tiles_n = (N + bn - 1) / bn;
+  // work tiles along N: the shared-A kernel takes two adjacent tiles at a time
+  // (the second past the last column when the count is odd: computed, not stored)
+  const int64_t tiles_n = ((N + bn - 1) / bn + plan.pairs - 1) / plan.pairs;
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
@@ -510,7 +520,9 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
                                  : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const uint32_t bk = 128 / es;  // K elements per 128-byte row
-  if (p.a_tma && !encode_2d(&L.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda) * es, bk, 128))
+  // A box: 128 rows, or 64 where two pairs each load half a CTA's rows for both
+  if (p.a_tma && !encode_2d(&L.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda) * es, bk,
+                            (plan.pair && plan.pairs == 2) ? 64 : 128))
     return GEMM_ERR_DRIVER;
   if (p.b_tma) {
     bool ok;
@@ -525,6 +537,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   }
   L.b_kmajor = kmajor;
   L.pair = plan.pair;
+  L.pairs = plan.pairs;
   L.bn = bn;
   L.grid = plan.grid;
   L.threads = (p.a_tma && p.b_tma) ? 192 : 320;
@@ -532,12 +545,13 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
 
   // internal consistency of the derived launch parameters (a violation is a library bug)
   if (p.raster < 1 || p.num_kb < 1 || p.num_tiles < 1 || p.num_work < p.num_tiles || p.tail_segs < 1 ||
-      p.tail_segs > kMaxTailSegs || L.grid < 1 || (L.pair && (L.grid % 2 != 0)) || p.tiles_n < 1 || p.tiles_m < 1)
+      p.tail_segs > kMaxTailSegs || L.grid < 1 || (L.pair && (L.grid % (2 * L.pairs) != 0)) || p.tiles_n < 1 ||
+      p.tiles_m < 1 || (L.pair && L.pairs != 1 && L.pairs != 2) || (!L.pair && L.pairs != 1))
     return GEMM_ERR_LAUNCH;
   cudaError_t e = kind == KIND_TF32 ? launch_tf32(L) : kind == KIND_BF16 ? launch_bf16(L) : launch_f16(L);
   if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  const int32_t info[8] = {plan.pair ? 2 : 1, bn, p.raster, L.grid, p.tail_segs, plan.conc, p.tail_start,
+  const int32_t info[8] = {plan.pair ? 2 * plan.pairs : 1, bn, p.raster, L.grid, p.tail_segs, plan.conc, p.tail_start,
                            p.num_work};
   memcpy(t_last_plan, info, sizeof(info));
   return GEMM_OK;
@@ -650,10 +664,10 @@ int gemm_last_plan(int32_t* out) {
 }
 
 int gemm_set_tuning(int variant, int tile_n, int raster, int tail_split) {
-  if (variant < 0 || variant > 2 || raster < 0 || tail_split < 0 || tail_split > 2) return GEMM_ERR_INVALID_VALUE;
+  if (variant < 0 || variant > 3 || raster < 0 || tail_split < 0 || tail_split > 2) return GEMM_ERR_INVALID_VALUE;
   if (tile_n != 0) {
     bool ok = false;
-    if (variant != 2)
+    if (variant < 2)
       for (int w : dgt::kTileWidths) ok = ok || (w == tile_n);
     if (variant != 1)
       for (int w : dgt::kPairTileWidths) ok = ok || (w == tile_n);

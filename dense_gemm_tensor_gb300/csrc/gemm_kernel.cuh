@@ -435,9 +435,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 4) {
     // ---------------------------------------------------------------- TMA producer
-    // The whole warp walks the loop (addresses and coordinates stay
-    // warp-uniform); one elected lane issues.
-    if (!(p.debug & DEBUG_STALL_PRODUCER)) {
+    if (lane == 0 && !(p.debug & DEBUG_STALL_PRODUCER)) {
       const uint32_t tx = (p.a_tma ? Cf::A_BYTES : 0) + (p.b_tma ? Cf::B_BYTES : 0);
       int it = 0;
       bool ok = true;
@@ -447,86 +445,72 @@ __global__ void __launch_bounds__(320, 1)
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!warp_wait_phase(p, empty0 + 8 * s, ph ^ 1, ROLE_PRODUCER | (s << 8))) {
+          if (!wait_phase(p, empty0 + 8 * s, ph ^ 1, ROLE_PRODUCER | (s << 8))) {
             ok = false;
             break;
           }
           const uint32_t fb = full0 + 8 * s;
-          const uint32_t a_dst = sA + s * Cf::A_BYTES;
-          const uint32_t b_dst = sB + s * Cf::B_BYTES;
-          if (elect_one()) {
-            mbar_arrive_expect_tx(fb, tx);
-            if (p.a_tma) tma_load_2d(a_dst, &tmA, fb, kb * Cf::BK, mb * Cf::BM);
-            if (p.b_tma) {
-              if constexpr (B_KMAJOR) {
-                tma_load_2d(b_dst, &tmB, fb, kb * Cf::BK, nb * Cf::BN);
-              } else {
+          mbar_arrive_expect_tx(fb, tx);
+          if (p.a_tma) tma_load_2d(sA + s * Cf::A_BYTES, &tmA, fb, kb * Cf::BK, mb * Cf::BM);
+          if (p.b_tma) {
+            if constexpr (B_KMAJOR) {
+              tma_load_2d(sB + s * Cf::B_BYTES, &tmB, fb, kb * Cf::BK, nb * Cf::BN);
+            } else {
 #pragma unroll
-                for (int j = 0; j < Cf::NBOX; ++j)
-                  tma_load_2d(b_dst + j * Cf::BOX_BYTES, &tmB, fb, nb * Cf::BN + j * Cf::BOXN, kb * Cf::BK);
-              }
+              for (int j = 0; j < Cf::NBOX; ++j)
+                tma_load_2d(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, nb * Cf::BN + j * Cf::BOXN,
+                            kb * Cf::BK);
             }
           }
-          __syncwarp();
         }
       }
-      if (lane == 0) *issued_slot = it;
+      *issued_slot = it;
     }
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer
-    // The whole warp walks the loop and builds the descriptors (warp-uniform);
-    // one elected lane -- the same lane every time -- issues the MMAs and commits.
-    int it = 0, tc = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tc) {
-      const int b = tc & 1;
-      const uint32_t use = (tc >> 1) & 1;
-      if (!warp_wait_phase(p, acce0 + 8 * b, use ^ 1, ROLE_MMA | (0x80u << 8))) break;
-      tc_fence_after();
-      const uint32_t d = tmem + b * Cf::ACC_COLS;
-      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-        const int s = it % S;
-        const uint32_t ph = (it / S) & 1;
-        if (!warp_wait_phase(p, full0 + 8 * s, ph, ROLE_MMA | (s << 8))) {
-          ok = false;
-          break;
-        }
+    if (lane == 0) {
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tc) {
+        const int b = tc & 1;
+        const uint32_t use = (tc >> 1) & 1;
+        if (!wait_phase(p, acce0 + 8 * b, use ^ 1, ROLE_MMA | (0x80u << 8))) break;
         tc_fence_after();
-        const uint32_t a_addr = sA + s * Cf::A_BYTES;
-        const uint32_t b_addr = sB + s * Cf::B_BYTES;
-        uint64_t ad[Cf::KSTEPS], bd[Cf::KSTEPS];
-#pragma unroll
-        for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
-          ad[kk] = sdesc(a_addr + kk * 32, 16, 1024, SWZ_128B);
-          if constexpr (B_KMAJOR)
-            bd[kk] = sdesc(b_addr + kk * 32, 16, 1024, SWZ_128B);
-          else
-            bd[kk] = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
-        }
-        const uint32_t first = kb == 0 ? 0u : 1u;
-        if (elect_one()) {
+        const uint32_t d = tmem + b * Cf::ACC_COLS;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!wait_phase(p, full0 + 8 * s, ph, ROLE_MMA | (s << 8))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sA + s * Cf::A_BYTES;
+          const uint32_t b_addr = sB + s * Cf::B_BYTES;
 #pragma unroll
           for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
-            const uint32_t acc = kk > 0 ? 1u : first;
-            if constexpr (KIND == KIND_TF32)
-              mma_tf32(d, ad[kk], bd[kk], Cf::IDESC, acc);
+            const uint64_t ad = sdesc(a_addr + kk * 32, 16, 1024, SWZ_128B);
+            uint64_t bd;
+            if constexpr (B_KMAJOR)
+              bd = sdesc(b_addr + kk * 32, 16, 1024, SWZ_128B);
             else
-              mma_f16(d, ad[kk], bd[kk], Cf::IDESC, acc);
+              bd = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            if constexpr (KIND == KIND_TF32)
+              mma_tf32(d, ad, bd, Cf::IDESC, acc);
+            else
+              mma_f16(d, ad, bd, Cf::IDESC, acc);
           }
           mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs have read it
         }
-        __syncwarp();
+        if (!ok) break;
+        mma_commit(accf0 + 8 * b);  // accumulator ready for the epilogue
       }
-      if (!ok) break;
-      if (elect_one()) mma_commit(accf0 + 8 * b);  // accumulator ready for the epilogue
-      __syncwarp();
+      *consumed_slot = it;
+      // wait for every MMA this thread issued (normally already complete)
+      mma_commit(drain_bar);
+      wait_phase_drain(p, drain_bar, 0);
     }
-    if (lane == 0) *consumed_slot = it;
-    // wait for every MMA issued (normally already complete)
-    if (elect_one()) mma_commit(drain_bar);
-    __syncwarp();
-    if (lane == 0) wait_phase_drain(p, drain_bar, 0);
-    __syncwarp();
   } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue
     int tc = 0;

@@ -9,6 +9,13 @@
 // both CTAs' shared memory at the same offsets and leaves rows 0-127 of the
 // accumulator in the leader's tensor memory and rows 128-255 in the peer's.
 //
+// PAIRS = 2: a cluster of four CTAs holds two pairs (ranks 0-1 and 2-3) that
+// compute two adjacent tiles of one 256-row band. CTAs of the same half (ranks
+// r and r + 2) need the same 128 rows of A, so each loads 64 of them and TMA
+// multicasts them into both; a stage is refilled only once both pairs' MMAs
+// have read it. A work tile is then two 256 x BN tiles; when the number of tile
+// columns is odd the second pair's last tile lies past N and is not stored.
+//
 // Tail: when the tiles do not fill a whole number of rounds of the grid, each
 // tile of the last partial round is split into `tail_segs` ranges of k-slabs
 // run by different pairs, so the round takes 1/tail_segs of a tile's time.
@@ -17,12 +24,13 @@
 // (its own from tensor memory) and stores C. No CTA waits for another, and
 // the sum does not depend on the arrival order.
 //
-// Synchronisation:
-//   full[s]   leader only; 1 arrival (leader producer, expecting the bytes of
-//             both CTAs' TMA loads, which all complete on this barrier)
-//   empty[s]  both CTAs; 1 arrival from the leader's commit (multicast)
-//   accf[b]   both CTAs; 1 arrival from the leader's commit (multicast)
-//   acce[b]   leader only; 8 arrivals (4 epilogue warps of each CTA)
+// Synchronisation (per pair; "leader" = the pair's even rank):
+//   full[s]   leader only; 1 arrival (leader producer, expecting the bytes that
+//             land in both CTAs of the pair, which all complete on this barrier)
+//   empty[s]  every CTA; PAIRS arrivals, one commit from each pair's leader
+//             (multicast to every CTA of the cluster)
+//   accf[b]   both CTAs of the pair; 1 arrival from the leader's commit (multicast)
+//   acce[b]   leader only; 8 arrivals (4 epilogue warps of each CTA of the pair)
 // Every wait is bounded as in the single-CTA kernel.
 #pragma once
 
@@ -112,13 +120,15 @@ __device__ __forceinline__ int arrive_split(const GemmParams& p, unsigned long l
 
 __device__ __forceinline__ void epilogue_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-template <int KIND, bool B_KMAJOR, int BN>
+template <int KIND, bool B_KMAJOR, int BN, int PAIRS>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmParams p) {
   using Cf = PairCfg<KIND, B_KMAJOR, BN>;
   constexpr int S = Cf::STAGES;
   constexpr int NB = Cf::ACC_BUFS;
+  constexpr int CL = 2 * PAIRS;  // CTAs per cluster
+  static_assert(PAIRS == 1 || PAIRS == 2, "one pair, or two pairs sharing A");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -140,15 +150,18 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  const int pair = blockIdx.x >> 1;
-  const int npairs = gridDim.x >> 1;
+  const uint32_t rank = cluster_ctarank();  // 0 .. CL-1
+  const uint32_t half = rank & 1u;           // which half of the pair's 256 rows
+  const uint32_t lead = rank & ~1u;          // rank of this pair's leader
+  const int q = int(rank >> 1);              // which pair of the cluster
+  const bool leader = half == 0;
+  const int pair = blockIdx.x / CL;          // the cluster's index in the work stream
+  const int npairs = gridDim.x / CL;
 
   if (warp == 4 && lane == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, PAIRS);  // one commit from each pair that reads stage s's A
     }
     for (int b = 0; b < NB; ++b) {
       mbar_init(accf0 + 8 * b, 1);
@@ -180,8 +193,8 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int w = pair; ok && w < p.num_work; w += npairs) {
         const PairWork wk = pair_work(p, w);
-        const int row0 = wk.mb * Cf::BMP + int(rank) * Cf::BM;
-        const int col0 = wk.nb * BN + int(rank) * Cf::BNH;
+        const int row0 = wk.mb * Cf::BMP + int(half) * Cf::BM;
+        const int col0 = (wk.nb * PAIRS + q) * BN + int(half) * Cf::BNH;
         for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -189,12 +202,19 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = mapa_shared(full0 + 8 * s, 0);
+          const uint32_t fb = mapa_shared(full0 + 8 * s, lead);
           const uint32_t a_dst = sA + s * Cf::A_BYTES;
           const uint32_t b_dst = sB + s * Cf::B_BYTES;
           if (elect_one()) {
             if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_BYTES);
-            tma_load_2d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0);
+            if constexpr (PAIRS == 1) {
+              tma_load_2d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0);
+            } else {
+              // both pairs need these 128 rows of A: each loads 64 of them into
+              // the same place in its own and the other pair's CTA of this half
+              tma_load_2d_pair_mc(a_dst + q * (Cf::A_BYTES / 2), &tmA, fb, kb * Cf::BK, row0 + q * (Cf::BM / 2),
+                                  uint16_t(0x5u << half));
+            }
             if constexpr (B_KMAJOR) {
               tma_load_2d_pair(b_dst, &tmB, fb, kb * Cf::BK, col0);
             } else {
@@ -251,16 +271,17 @@ __global__ void __launch_bounds__(192, 1)
               else
                 mma_f16_pair(d, ad[kk], bd[kk], Cf::IDESC, acc);
             }
-            mma_commit_pair(empty0 + 8 * s, 0x3);  // both CTAs may refill stage s
+            // every CTA whose loads land in stage s may refill it once all pairs are done with it
+            mma_commit_pair(empty0 + 8 * s, uint16_t((1u << CL) - 1u));
           }
           __syncwarp();
         }
         if (!ok) break;
-        if (elect_one()) mma_commit_pair(accf0 + 8 * b, 0x3);  // both halves of the accumulator ready
+        if (elect_one()) mma_commit_pair(accf0 + 8 * b, uint16_t(0x3u << lead));  // both halves of the accumulator ready
         __syncwarp();
       }
       if (lane == 0) *consumed_slot = it;
-      if (elect_one()) mma_commit_pair(drain_bar, 0x1);
+      if (elect_one()) mma_commit_pair(drain_bar, uint16_t(1u << lead));
       __syncwarp();
       if (lane == 0) wait_phase_drain(p, drain_bar, 0);
       __syncwarp();
@@ -279,18 +300,19 @@ __global__ void __launch_bounds__(192, 1)
       epilogue_barrier();
       if (!ok_slot[tc & 1]) break;
       tc_fence_after();
-      const int row = wk.mb * Cf::BMP + int(rank) * Cf::BM + warp * 32 + lane;
+      const int nbt = wk.nb * PAIRS + q;  // this pair's tile column (past the last one: nothing to store)
+      const int row = wk.mb * Cf::BMP + int(half) * Cf::BM + warp * 32 + lane;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
-      const int ncols = min(BN, p.N - wk.nb * BN);
-      const int nchunks = (ncols + 31) / 32;
-      const int col0 = wk.nb * BN;
+      const int ncols = min(BN, p.N - nbt * BN);
+      const int nchunks = ncols > 0 ? (ncols + 31) / 32 : 0;
+      const int col0 = nbt * BN;
       if (wk.f < 0) {
         for_each_acc_chunk(taddr, nchunks,
                            [&](int c, const uint32_t(&r)[32]) { store_row_chunk<KIND>(p, row, col0 + c * 32, r); });
       } else {
         // split tile: publish this segment's partial, then find out whether it is the last
         float4* mine = reinterpret_cast<float4*>(
-            p.ws + (static_cast<long long>(wk.f * p.tail_segs + wk.seg) * 2 + rank) * Cf::PARTIAL_FLOATS);
+            p.ws + (static_cast<long long>(wk.f * p.tail_segs + wk.seg) * CL + rank) * Cf::PARTIAL_FLOATS);
         for_each_acc_chunk(taddr, nchunks, [&](int c, const uint32_t(&r)[32]) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -301,7 +323,7 @@ __global__ void __launch_bounds__(192, 1)
         __threadfence();
         epilogue_barrier();
         if (tid == 0) {
-          const int arrival = arrive_split(p, p.ws_ctr + wk.f * 2 + rank);
+          const int arrival = arrive_split(p, p.ws_ctr + wk.f * CL + rank);
           *last_slot = (arrival + 1 == p.tail_segs) ? 1 : 0;
         }
         epilogue_barrier();
@@ -310,7 +332,7 @@ __global__ void __launch_bounds__(192, 1)
         if (last && p.tail_segs == 2) {
           // C = own + other: fp32 addition commutes, so which segment arrives last does not matter
           const float4* other = reinterpret_cast<const float4*>(
-              p.ws + (static_cast<long long>(wk.f * 2 + (1 - wk.seg)) * 2 + rank) * Cf::PARTIAL_FLOATS);
+              p.ws + (static_cast<long long>(wk.f * 2 + (1 - wk.seg)) * CL + rank) * Cf::PARTIAL_FLOATS);
           float4 nxt[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) nxt[q] = __ldcg(other + q * 128 + tid);
@@ -345,7 +367,7 @@ __global__ void __launch_bounds__(192, 1)
                   acc[j] = (sg == 0) ? __uint_as_float(r[j]) : acc[j] + __uint_as_float(r[j]);
               } else {
                 const float4* part = reinterpret_cast<const float4*>(
-                    p.ws + (static_cast<long long>(wk.f * p.tail_segs + sg) * 2 + rank) * Cf::PARTIAL_FLOATS);
+                    p.ws + (static_cast<long long>(wk.f * p.tail_segs + sg) * CL + rank) * Cf::PARTIAL_FLOATS);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                   const float4 v = __ldcg(part + (c * 8 + q) * 128 + tid);
@@ -365,7 +387,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(acce0 + 8 * b, 0));
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(acce0 + 8 * b, lead));
     }
   }
 

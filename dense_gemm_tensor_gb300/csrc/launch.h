@@ -14,7 +14,8 @@ struct LaunchPlan {
   CUtensorMap tmB;  // valid when p.b_tma
   GemmParams p;
   bool b_kmajor;
-  bool pair;  // CTA-pair kernel (cluster of 2, cta_group::2)
+  bool pair;  // CTA-pair kernel (cta_group::2)
+  int pairs;  // pair kernel: CTA pairs per cluster (1, or 2 sharing A by multicast)
   int bn;     // output tile width: one of kTileWidths (single) or kPairTileWidths (pair)
   int grid;
   int threads;
@@ -24,18 +25,18 @@ struct LaunchPlan {
 cudaError_t launch_f16(const LaunchPlan& L);
 cudaError_t launch_bf16(const LaunchPlan& L);
 cudaError_t launch_tf32(const LaunchPlan& L);
-int pair_clusters_f16(bool kmajor, int bn);
-int pair_clusters_bf16(bool kmajor, int bn);
-int pair_clusters_tf32(bool kmajor, int bn);
+int pair_clusters_f16(bool kmajor, int bn, int pairs);
+int pair_clusters_bf16(bool kmajor, int bn, int pairs);
+int pair_clusters_tf32(bool kmajor, int bn, int pairs);
 cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count);
 // Copies rows of `row_bytes` from a source with `gran`-byte-aligned row starts
 // to a destination with 16-byte-aligned rows (pack_rows_kernel).
 cudaError_t launch_pack(const void* src, int64_t src_ld_bytes, void* dst, int64_t dst_ld_bytes, int64_t rows,
                         int64_t row_bytes, int gran, cudaStream_t stream, int sm_count);
 
-// Split-tail scratch layout: arrival counters for up to 1024 split tiles,
-// then the fp32 partial tiles.
-constexpr size_t kSplitCounterBytes = 1024 * 2 * sizeof(unsigned long long);
+// Split-tail scratch layout: arrival counters (one per CTA of a cluster of up
+// to four) for up to 1024 split work tiles, then the fp32 partial tiles.
+constexpr size_t kSplitCounterBytes = 1024 * 4 * sizeof(unsigned long long);
 
 // Caller-owned scratch for the split tail (instead of the per-stream buffer
 // the library allocates): device address and capacity in bytes.
@@ -84,13 +85,13 @@ cudaError_t launch_layout(const LaunchPlan& L) {
 }
 
 
-template <int KIND, bool KMAJ, int BN>
+template <int KIND, bool KMAJ, int BN, int PAIRS>
 cudaError_t launch_pair_variant(const LaunchPlan& L) {
   static int configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_kernel_pair<KIND, KMAJ, BN>;
+  auto kern = gemm_kernel_pair<KIND, KMAJ, BN, PAIRS>;
   constexpr int smem = PairCfg<KIND, KMAJ, BN>::SMEM_BYTES;
   if (dev >= 64 || !__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -100,7 +101,7 @@ cudaError_t launch_pair_variant(const LaunchPlan& L) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = 2 * PAIRS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(L.grid, 1, 1);
@@ -115,9 +116,9 @@ cudaError_t launch_pair_variant(const LaunchPlan& L) {
 }
 
 // Co-resident clusters of one pair variant (occupancy query with its launch shape).
-template <int KIND, bool KMAJ, int BN>
+template <int KIND, bool KMAJ, int BN, int PAIRS>
 int pair_clusters_variant() {
-  auto kern = gemm_kernel_pair<KIND, KMAJ, BN>;
+  auto kern = gemm_kernel_pair<KIND, KMAJ, BN, PAIRS>;
   constexpr int smem = PairCfg<KIND, KMAJ, BN>::SMEM_BYTES;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
     cudaGetLastError();
@@ -126,10 +127,10 @@ int pair_clusters_variant() {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = 2 * PAIRS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(2, 1, 1);
+  cfg.gridDim = dim3(2 * PAIRS, 1, 1);
   cfg.blockDim = dim3(192, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.attrs = attr;
@@ -142,31 +143,40 @@ int pair_clusters_variant() {
   return n;
 }
 
-template <int KIND, bool KMAJ>
-cudaError_t launch_pair_layout(const LaunchPlan& L) {
+template <int KIND, bool KMAJ, int PAIRS>
+cudaError_t launch_pair_width(const LaunchPlan& L) {
   switch (L.bn) {
-    case 256: return launch_pair_variant<KIND, KMAJ, 256>(L);
-    case 224: return launch_pair_variant<KIND, KMAJ, 224>(L);
-    case 192: return launch_pair_variant<KIND, KMAJ, 192>(L);
-    case 128: return launch_pair_variant<KIND, KMAJ, 128>(L);
+    case 256: return launch_pair_variant<KIND, KMAJ, 256, PAIRS>(L);
+    case 224: return launch_pair_variant<KIND, KMAJ, 224, PAIRS>(L);
+    case 192: return launch_pair_variant<KIND, KMAJ, 192, PAIRS>(L);
+    case 128: return launch_pair_variant<KIND, KMAJ, 128, PAIRS>(L);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int KIND, bool KMAJ>
-int pair_clusters_layout(int bn) {
+cudaError_t launch_pair_layout(const LaunchPlan& L) {
+  if (L.pairs == 1) return launch_pair_width<KIND, KMAJ, 1>(L);
+  if (L.pairs == 2) return launch_pair_width<KIND, KMAJ, 2>(L);
+  return cudaErrorInvalidValue;
+}
+
+template <int KIND, bool KMAJ, int PAIRS>
+int pair_clusters_width(int bn) {
   switch (bn) {
-    case 256: return pair_clusters_variant<KIND, KMAJ, 256>();
-    case 224: return pair_clusters_variant<KIND, KMAJ, 224>();
-    case 192: return pair_clusters_variant<KIND, KMAJ, 192>();
-    case 128: return pair_clusters_variant<KIND, KMAJ, 128>();
+    case 256: return pair_clusters_variant<KIND, KMAJ, 256, PAIRS>();
+    case 224: return pair_clusters_variant<KIND, KMAJ, 224, PAIRS>();
+    case 192: return pair_clusters_variant<KIND, KMAJ, 192, PAIRS>();
+    case 128: return pair_clusters_variant<KIND, KMAJ, 128, PAIRS>();
     default: return 0;
   }
 }
 
 template <int KIND>
-int pair_clusters_kind(bool kmajor, int bn) {
-  return kmajor ? pair_clusters_layout<KIND, true>(bn) : pair_clusters_layout<KIND, false>(bn);
+int pair_clusters_kind(bool kmajor, int bn, int pairs) {
+  if (pairs == 1) return kmajor ? pair_clusters_width<KIND, true, 1>(bn) : pair_clusters_width<KIND, false, 1>(bn);
+  if (pairs == 2) return kmajor ? pair_clusters_width<KIND, true, 2>(bn) : pair_clusters_width<KIND, false, 2>(bn);
+  return 0;
 }
 
 template <int KIND>

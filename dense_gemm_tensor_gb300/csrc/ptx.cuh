@@ -225,6 +225,19 @@ __device__ __forceinline__ void mma_tf32_pair(uint32_t d, uint64_t a, uint64_t b
 
 // Arrive once on the mbarrier at CTA-local offset `bar` in every CTA of
 // `cta_mask` when this thread's earlier pair MMAs have completed.
+// 2-D tiled TMA load multicast to the CTAs of `cta_mask` (the data lands at
+// offset `dst` of each). With .cta_group::2 each destination's completion is
+// signalled on the barrier at the offset of `bar_cluster` in the leader (even
+// rank) CTA of that destination's pair, so `bar_cluster` names a leader's barrier.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t x,
+                                                    int32_t y, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "h"(cta_mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),

@@ -161,7 +161,7 @@ uint64_t gemm_launch_count(void);
 /*
  * The launch plan of the calling host thread's last GEMM call that launched
  * the product kernel, as 8 integers in out[0..7]: kernel (1 single CTA, 2 CTA
- * pair), tile width, band height, grid size in CTAs, K segments per tile of
+ * pair, 4 two CTA pairs sharing A), tile width, band height, grid size in CTAs, K segments per tile of
  * the last partial round (1 = not split), tiles in flight at once, first
  * split tile, number of work items. All zero before the first such call.
  */
@@ -170,9 +170,10 @@ int gemm_last_plan(int32_t* out);
 /*
  * Tuning hook, process-wide, for subsequent calls. `variant`: 0 = chosen per
  * call, 1 = single-CTA kernel (128-row tiles), 2 = CTA-pair kernel (256-row
- * tiles; only when A and B rows are 16-byte aligned, else the single-CTA
- * kernel runs). `tile_n`: output tile width, 256, 224, 192 or 128 for the
- * single-CTA kernel and 256, 224, 192 or 128 for the pair (0 = chosen per call).
+ * tiles), 3 = clusters of two CTA pairs that take two adjacent 256-row tiles
+ * and load their shared A rows once, by TMA multicast (2 and 3 only when A
+ * and B rows are 16-byte aligned or can be packed, else the single-CTA kernel
+ * runs). `tile_n`: output tile width, 256, 224, 192 or 128 (0 = chosen per call).
  * `raster`: band height of the tile order in tile rows (0 = chosen per call).
  * `tail_split`: 0 or 2 = split the tiles of the last partial round along K
  * where the shape allows (the default), 1 = never split.
