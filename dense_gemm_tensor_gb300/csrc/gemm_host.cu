@@ -421,17 +421,27 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   const bool kmajor = layout == GEMM_B_K_MAJOR;
   int dev_id = 0;
   cudaGetDevice(&dev_id);
-  // Operands whose rows TMA cannot address are packed into 16-byte-aligned
-  // rows in the stream's scratch first (a bandwidth-bound copy), so that the
-  // TMA kernels run; without scratch the kernel's copy warps read them in place.
+  // Operands whose rows TMA cannot address (row starts not 16-byte aligned)
+  // are packed into 128-byte-aligned rows in the stream's scratch first (a
+  // bandwidth-bound copy), so that the TMA kernels run; without scratch the
+  // kernel's copy warps read them in place. In a large product an operand is
+  // also packed when its rows are TMA-legal but do not start on 128-byte
+  // boundaries: each 128-byte row of its boxes then straddles two L2 lines,
+  // and the k-loop ran about a third slower (4000 x 4100 x 4104 on GB300). The
+  // copy pays for itself once the other output dimension is a few thousand.
   const bool may_pack = ext == nullptr && !(g_debug_flags.load(std::memory_order_relaxed) & DEBUG_NO_PACK);
-  const bool pack_a = may_pack && ga < 16, pack_b = may_pack && gb < 16;
+  auto off_line = [es](const void* ptr, int64_t ld) {
+    return ((reinterpret_cast<uintptr_t>(ptr) | static_cast<uintptr_t>(ld * es)) % 128) != 0;
+  };
+  const bool big = 2.0 * double(M) * double(N) * double(K) >= 1.6e10;
+  const bool pack_a = may_pack && (ga < 16 || (big && N >= 2048 && off_line(A, lda)));
+  const bool pack_b = may_pack && (gb < 16 || (big && M >= 2048 && off_line(B, ldb)));
   TilePlan plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, (ga == 16 || pack_a) && (gb == 16 || pack_b),
                               dev->sm_count);
   // Scratch for this plan, laid out as [counters][split partials][packed A][packed B].
-  const int64_t lda_p = pack_a ? (K + 16 / es - 1) / (16 / es) * (16 / es) : lda;
+  const int64_t lda_p = pack_a ? (K * es + 127) / 128 * 128 / es : lda;
   const int64_t b_rows = kmajor ? N : K, b_cols = kmajor ? K : N;
-  const int64_t ldb_p = pack_b ? (b_cols + 16 / es - 1) / (16 / es) * (16 / es) : ldb;
+  const int64_t ldb_p = pack_b ? (b_cols * es + 127) / 128 * 128 / es : ldb;
   auto split_tiles = [&](const TilePlan& pl) {
     const int64_t tm = (M + (pl.pair ? 255 : 127)) / (pl.pair ? 256 : 128);
     const int64_t tn = ((N + pl.bn - 1) / pl.bn + pl.pairs - 1) / pl.pairs;
@@ -508,7 +518,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   if (!p.a_tma) p.copy_bytes = ga;
   if (!p.b_tma && gb < p.copy_bytes) p.copy_bytes = gb;
   p.c_gran = granularity(C, ldc, es);
-  p.c_vec = p.c_gran == 16;
+  p.c_tma = p.c_gran == 16;
   p.status = dev->status_words;
   uint32_t ep = g_epoch.fetch_add(1, std::memory_order_relaxed);
   if (ep == 0) ep = g_epoch.fetch_add(1, std::memory_order_relaxed);
@@ -535,6 +545,10 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     }
     if (!ok) return GEMM_ERR_DRIVER;
   }
+  // C box: 32 rows x 64 bytes, the staging tile of one epilogue warp (64-byte swizzle)
+  if (p.c_tma && !encode_2d(&L.tmC, dt, C, uint64_t(N), uint64_t(M), uint64_t(ldc) * es, uint32_t(64 / es), 32,
+                            CU_TENSOR_MAP_SWIZZLE_64B))
+    return GEMM_ERR_DRIVER;
   L.b_kmajor = kmajor;
   L.pair = plan.pair;
   L.pairs = plan.pairs;

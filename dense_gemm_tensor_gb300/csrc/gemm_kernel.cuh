@@ -98,13 +98,17 @@ struct GemmParams {
   long long ldc;
   int a_tma, b_tma;  // operand loaded by TMA (1) or by the copy warps (0)
   int copy_bytes;    // copy-warp granularity in bytes: 16, 8, 4 or 2
-  int c_vec;         // C base and row pitch allow 16-byte stores
+  int c_tma;         // C written by TMA stores (base and row pitch are 16-byte multiples)
   int c_gran;        // widest store (bytes: 16, 8, 4 or 2) the C base and row pitch allow
   uint32_t* status;  // device status words [2]
   uint32_t epoch;    // unique per launch
   uint32_t debug;
   unsigned long long wait_limit_ns;
 };
+
+// Output staging in shared memory: 2 KB per epilogue warp (see epi_round).
+constexpr int EPI_WARP_BYTES = 32 * 64;
+constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
 
 template <int KIND, bool B_KMAJOR, int BN_>
 struct Cfg {
@@ -127,7 +131,7 @@ struct Cfg {
   static constexpr uint32_t B_SBO = B_ATOM32 ? DGT_ATOM32_SBO : 1024;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SMEM_LIMIT = 232448;  // opt-in dynamic shared memory per block
-  static constexpr int RESERVED = 1024 /*align slack*/ + 256 /*barriers*/;
+  static constexpr int RESERVED = 1024 /*align slack*/ + EPI_BYTES /*output staging*/ + 256 /*barriers*/;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int ACC_COLS = BN;       // fp32 accumulator columns of one buffer
@@ -139,6 +143,7 @@ struct Cfg {
   static_assert(STAGES >= 3, "pipeline depth");
   static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
 
   // Instruction descriptor: D fp32, A/B format, A K-major, B K- or MN-major, N, M.
   static constexpr uint32_t IDESC = (1u << 4) | (KindTraits<KIND>::fmt << 7) | (KindTraits<KIND>::fmt << 10) |
@@ -297,61 +302,84 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
   }
 }
 
+// Each epilogue warp owns a 32-row x 64-byte tile of shared memory in the
+// layout of TMA's 64-byte swizzle: 16-byte chunk j of row r sits at
+// r * 64 + ((j ^ ((r >> 1) & 3)) * 16), so both the lanes' row writes (lane =
+// row) and the row-wise reads below are free of bank conflicts. One round
+// stages 64 bytes of each of the warp's 32 rows -- 32 columns of a 16-bit C,
+// 16 of an fp32 C -- and writes them to C[row0 .., col0 ..]: by one TMA store
+// of the 32 x 64-byte box when C's base and row pitch are 16-byte multiples
+// and the box ends at or before column N (TMA leaves out the rows past M; a
+// box that crosses column N wrote whole 16-byte pieces past it on GB300, so
+// that last round of a row goes the other way), otherwise by coalesced stores,
+// 16 lanes to a row and two rows a step, 4 bytes a lane where C's alignment
+// allows and 2 where it does not.
+__device__ __forceinline__ uint32_t epi_chunk_addr(uint32_t stage, int r, int j) {
+  return stage + static_cast<uint32_t>(r * 64) + (static_cast<uint32_t>(j ^ ((r >> 1) & 3)) << 4);
+}
+
 template <int KIND>
-__device__ __forceinline__ void store_one(void* C, long long idx, uint32_t bits) {
+__device__ __forceinline__ void epi_round(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage, int lane,
+                                          int row0, int col0, const uint32_t (&w)[16]) {
+  // the previous round's TMA store must have read the tile (only lane 0 has stores in flight)
+  if (p.c_tma && lane == 0) bulk_wait_read_all();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) st_shared_v4(epi_chunk_addr(stage, lane, j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  constexpr int ROUND_COLS = KIND == KIND_TF32 ? 16 : 32;
+  if (p.c_tma && col0 + ROUND_COLS <= p.N) {
+    fence_proxy_async_smem();  // make the tile visible to the TMA unit
+    __syncwarp();
+    if (lane == 0 && row0 < p.M && col0 < p.N) {
+      tma_store_2d(tmC, stage, col0, row0);
+      bulk_commit_group();
+    }
+  } else {
+    __syncwarp();
+    constexpr int ES = KIND == KIND_TF32 ? 4 : 2;
+    const int l = lane & 15;
+    const int col = col0 + l * (4 / ES);
+#pragma unroll 4
+    for (int rr = 0; rr < 32; rr += 2) {
+      const int r = rr + (lane >> 4);
+      const int row = row0 + r;
+      const uint32_t v = ld_shared_u32(epi_chunk_addr(stage, r, l >> 2) + ((l & 3) << 2));
+      if (row < p.M && col < p.N) {
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.C) + (static_cast<long long>(row) * p.ldc + col) * ES;
+        if (ES == 4 || (p.c_gran >= 4 && col + 1 < p.N)) {
+          *reinterpret_cast<uint32_t*>(dst) = v;
+        } else {
+          reinterpret_cast<uint16_t*>(dst)[0] = static_cast<uint16_t>(v & 0xFFFFu);
+          if (col + 1 < p.N) reinterpret_cast<uint16_t*>(dst)[1] = static_cast<uint16_t>(v >> 16);
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// Converts 32 accumulator columns of the warp's 32 rows (lane = row, values
+// in r) to the output type and writes them to C[row0 .., col0 .. col0+31].
+// Warp-collective.
+template <int KIND>
+__device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage, int lane,
+                                           int row0, int col0, const uint32_t (&r)[32]) {
   if constexpr (KIND == KIND_TF32) {
-    reinterpret_cast<uint32_t*>(C)[idx] = bits;
-  } else if constexpr (KIND == KIND_BF16) {
-    reinterpret_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(__uint_as_float(bits));
-  } else {
-    reinterpret_cast<__half*>(C)[idx] = __float2half_rn(__uint_as_float(bits));
-  }
-}
-
-// 32 accumulator columns of one row -> C[row][col0 .. col0+31].
-template <int KIND>
-__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, int col0, const uint32_t (&r)[32]) {
-  if (row < 0 || row >= p.M || col0 < 0 || col0 >= p.N) return;
-  const long long idx0 = static_cast<long long>(row) * p.ldc + col0;
-  if (p.c_vec && col0 + 32 <= p.N) {
-    if constexpr (KIND == KIND_TF32) {
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(p.C) + idx0);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) dst[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-    } else {
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.C) + idx0);
+    for (int h = 0; h < 2; ++h) {
+      if (col0 + 16 * h >= p.N) break;
+      uint32_t w[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        dst[q] = make_uint4(pack2<KIND>(r[8 * q], r[8 * q + 1]), pack2<KIND>(r[8 * q + 2], r[8 * q + 3]),
-                            pack2<KIND>(r[8 * q + 4], r[8 * q + 5]), pack2<KIND>(r[8 * q + 6], r[8 * q + 7]));
-    }
-  } else if (p.c_gran >= 4 && col0 + 32 <= p.N) {
-    // unaligned rows: the widest stores the row start allows (4 or 8 bytes)
-    uint32_t w[KIND == KIND_TF32 ? 32 : 16];
-    if constexpr (KIND == KIND_TF32) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) w[j] = r[j];
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = pack2<KIND>(r[2 * j], r[2 * j + 1]);
-    }
-    constexpr int NW = KIND == KIND_TF32 ? 32 : 16;
-    uint8_t* dst = reinterpret_cast<uint8_t*>(p.C) + idx0 * (KIND == KIND_TF32 ? 4 : 2);
-    if (p.c_gran >= 8) {
-#pragma unroll
-      for (int j = 0; j < NW / 2; ++j) reinterpret_cast<uint2*>(dst)[j] = make_uint2(w[2 * j], w[2 * j + 1]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < NW; ++j) reinterpret_cast<uint32_t*>(dst)[j] = w[j];
+      for (int j = 0; j < 16; ++j) w[j] = r[16 * h + j];
+      epi_round<KIND>(p, tmC, stage, lane, row0, col0 + 16 * h, w);
     }
   } else {
-    const int lim = min(32, p.N - col0);
+    uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < lim) store_one<KIND>(p.C, idx0 + j, r[j]);
+    for (int j = 0; j < 16; ++j) w[j] = pack2<KIND>(r[2 * j], r[2 * j + 1]);
+    epi_round<KIND>(p, tmC, stage, lane, row0, col0, w);
   }
 }
-
 
 // Reads `nchunks` 32-column chunks of this warp's 32 accumulator rows from
 // tensor memory and hands each to `use(c, r)`, keeping the next chunk's load
@@ -383,7 +411,7 @@ __device__ __forceinline__ void for_each_acc_chunk(uint32_t taddr, int nchunks, 
 template <int KIND, bool B_KMAJOR, int BN>
 __global__ void __launch_bounds__(320, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using Cf = Cfg<KIND, B_KMAJOR, BN>;
   constexpr int S = Cf::STAGES;
 
@@ -393,7 +421,8 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sptr = smem_raw + (sbase - raw);
   const uint32_t sA = sbase;
   const uint32_t sB = sbase + S * Cf::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sptr + S * (Cf::A_BYTES + Cf::B_BYTES));
+  const uint32_t sE = sbase + S * (Cf::A_BYTES + Cf::B_BYTES);  // output staging, EPI_BYTES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sptr + S * (Cf::A_BYTES + Cf::B_BYTES) + EPI_BYTES);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
   const uint32_t accf0 = empty0 + 8 * S;
@@ -521,15 +550,19 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t use = (tc >> 1) & 1;
       if (!warp_wait_phase(p, accf0 + 8 * b, use, ROLE_EPILOGUE | (b << 8))) break;
       tc_fence_after();
-      const int row = mb * Cf::BM + warp * 32 + lane;
+      const int row0 = mb * Cf::BM + warp * 32;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
       const int ncols = min(Cf::BN, p.N - nb * Cf::BN);
-      for_each_acc_chunk(taddr, (ncols + 31) / 32,
-                         [&](int c, const uint32_t(&r)[32]) { store_row_chunk<KIND>(p, row, nb * Cf::BN + c * 32, r); });
+      const uint32_t stage = sE + warp * EPI_WARP_BYTES;
+      for_each_acc_chunk(taddr, (ncols + 31) / 32, [&](int c, const uint32_t(&r)[32]) {
+        emit_chunk<KIND>(p, &tmC, stage, lane, row0, nb * Cf::BN + c * 32, r);
+      });
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * b);
     }
+    if (lane == 0) bulk_wait_all();  // this warp's TMA stores of C have completed
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- copy warps (6-9)
     const int ctid = threadIdx.x - 6 * 32;  // 0..127

@@ -59,7 +59,7 @@ struct PairCfg {
   static constexpr uint32_t B_SBO = B_ATOM32 ? DGT_ATOM32_SBO : 1024;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SMEM_LIMIT = 232448;
-  static constexpr int RESERVED = 1024 + 256;
+  static constexpr int RESERVED = 1024 /*align slack*/ + EPI_BYTES /*output staging*/ + 256 /*barriers*/;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int ACC_BUFS = 2;  // the epilogue of one tile overlaps the next tile's k-loop
@@ -73,6 +73,7 @@ struct PairCfg {
   static_assert(ACC_BUFS * BN <= 512, "tensor memory");
   static_assert(NUM_BARS * 8 + 32 <= 256, "barrier area");
   static_assert(STAGES >= 3, "pipeline depth");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
   static constexpr uint32_t IDESC = (1u << 4) | (KindTraits<KIND>::fmt << 7) | (KindTraits<KIND>::fmt << 10) |
                                     ((B_KMAJOR ? 0u : 1u) << 16) | (uint32_t(BN >> 3) << 17) |
                                     (uint32_t(BMP >> 4) << 24);
@@ -123,7 +124,7 @@ __device__ __forceinline__ void epilogue_barrier() { asm volatile("bar.sync 1, 1
 template <int KIND, bool B_KMAJOR, int BN, int PAIRS>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using Cf = PairCfg<KIND, B_KMAJOR, BN>;
   constexpr int S = Cf::STAGES;
   constexpr int NB = Cf::ACC_BUFS;
@@ -136,7 +137,8 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sptr = smem_raw + (sbase - raw);
   const uint32_t sA = sbase;
   const uint32_t sB = sbase + S * Cf::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sptr + S * Cf::STAGE_BYTES);
+  const uint32_t sE = sbase + S * Cf::STAGE_BYTES;  // output staging, EPI_BYTES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sptr + S * Cf::STAGE_BYTES + EPI_BYTES);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
   const uint32_t accf0 = empty0 + 8 * S;
@@ -301,14 +303,15 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok_slot[tc & 1]) break;
       tc_fence_after();
       const int nbt = wk.nb * PAIRS + q;  // this pair's tile column (past the last one: nothing to store)
-      const int row = wk.mb * Cf::BMP + int(half) * Cf::BM + warp * 32 + lane;
+      const int row0 = wk.mb * Cf::BMP + int(half) * Cf::BM + warp * 32;  // first of this warp's 32 rows
+      const uint32_t stage = sE + warp * EPI_WARP_BYTES;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
       const int ncols = min(BN, p.N - nbt * BN);
       const int nchunks = ncols > 0 ? (ncols + 31) / 32 : 0;
       const int col0 = nbt * BN;
       if (wk.f < 0) {
         for_each_acc_chunk(taddr, nchunks,
-                           [&](int c, const uint32_t(&r)[32]) { store_row_chunk<KIND>(p, row, col0 + c * 32, r); });
+                           [&](int c, const uint32_t(&r)[32]) { emit_chunk<KIND>(p, &tmC, stage, lane, row0, col0 + c * 32, r); });
       } else {
         // split tile: publish this segment's partial, then find out whether it is the last
         float4* mine = reinterpret_cast<float4*>(
@@ -352,7 +355,7 @@ __global__ void __launch_bounds__(192, 1)
               sum[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + cur[q].z);
               sum[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + cur[q].w);
             }
-            store_row_chunk<KIND>(p, row, col0 + c * 32, sum);
+            emit_chunk<KIND>(p, &tmC, stage, lane, row0, col0 + c * 32, sum);
           });
         } else if (last) {
           // three or four segments: add them in segment order; this CTA's own one comes from tensor memory
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t out[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) out[j] = __float_as_uint(acc[j]);
-            store_row_chunk<KIND>(p, row, col0 + c * 32, out);
+            emit_chunk<KIND>(p, &tmC, stage, lane, row0, col0 + c * 32, out);
           });
         }
       }
@@ -389,6 +392,8 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(acce0 + 8 * b, lead));
     }
+    if (lane == 0) bulk_wait_all();  // this warp's TMA stores of C have completed
+    __syncwarp();
   }
 
   // ------------------------------------------------------------------ teardown
