@@ -161,6 +161,13 @@ def run_ours(args, world, rank, local):
         for _ in range(args.warmup):
             step()
     stream.synchronize()
+    # the launch plan of each product (the same every step: it depends only on shape and alignment)
+    plans = {}
+    with torch.cuda.stream(stream):
+        for dt in DTYPES:
+            gemm.matmul(A[dt], B[dt], C[dt], stream=stream)
+            plans[dt] = gemm.last_plan()
+    stream.synchronize()
     if gemm.device_status(stream) != 0:
         raise RuntimeError("device status word set during warm-up")
 
@@ -240,7 +247,8 @@ def run_ours(args, world, rank, local):
                    "l2": "no flush: each step streams 384 MiB of operands (3x the 129 MB L2), so a product's "
                          "inputs are evicted by the other two before it runs again"},
         "per_dtype": per_dtype,
-        "roofline": {"bound": "tensor", "kernel": f"gemm_kernel<{dominant}>",
+        "roofline": {"bound": "tensor", "kernel": kernel_name(dominant, plans[dominant]),
+                     "plan": {k: plans[dominant][k] for k in ("kernel", "tile_n", "raster", "tail_segs")},
                      "achieved": per_dtype[dominant]["tflops"], "peak": per_dtype[dominant]["peak_tflops"],
                      "unit": "TFLOP/s", "frac": per_dtype[dominant]["frac"], "traffic": None,
                      "peak_source": f"{peak_src} bf16 burst x nominal {dominant}/bf16 ratio"},
@@ -249,7 +257,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks.summary(),
         "gpu_launches": launches,
     }
-    traffic = _traffic_record(dominant)
+    traffic = _traffic_record(dominant, plans[dominant])
     if traffic is not None:
         line["roofline"]["traffic"] = traffic
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -259,21 +267,35 @@ def run_ours(args, world, rank, local):
     return line, rank
 
 
+KIND_INDEX = {"f16": 0, "bf16": 1, "tf32": 2}
+
+
+def kernel_name(dtype, plan):
+    """The product kernel a plan launches, as ncu names it (row-major B)."""
+    k, bn = plan["kernel"], plan["tile_n"]
+    if k == 1:
+        return f"gemm_kernel<{KIND_INDEX[dtype]}, 0, {bn}>"
+    return f"gemm_kernel_pair<{KIND_INDEX[dtype]}, 0, {bn}, {k // 2}>"
+
+
+# Device code of the product kernels: the traffic record holds while these are unchanged.
+KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_kernel_pair.cuh", "ptx.cuh")
+
+
 def _kernel_sources_sha256():
-    import glob
     import hashlib
     csrc = os.path.join(ROOT, "dense_gemm_tensor_gb300", "csrc")
-    paths = sorted(glob.glob(os.path.join(csrc, "*.cu*")) + glob.glob(os.path.join(csrc, "*.h")))
     h = hashlib.sha256()
-    for p in paths:
-        with open(p, "rb") as f:
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def _traffic_record(dtype):
+def _traffic_record(dtype, plan):
     """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) from the
-    committed summary, or None when the kernel sources changed since it was captured."""
+    committed summary, or None when the kernel's device code changed since it was captured
+    or this run's plan launched a different kernel."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -281,7 +303,11 @@ def _traffic_record(dtype):
         d = json.load(f)
     if d.get("kernel_sources_sha256") != _kernel_sources_sha256():
         return None
-    return d.get(dtype)
+    rec = d.get(dtype)
+    if not isinstance(rec, dict) or rec.get("kernel") != kernel_name(dtype, plan) or \
+            rec.get("tail_segs") != plan["tail_segs"]:
+        return None
+    return rec.get("bytes")
 
 
 def cpu_baseline(probs, seconds):

@@ -277,12 +277,12 @@ struct TilePlan {
 // width 256/224/192/128, measured on GB300 at 4096^3 (bf16; tf32 takes the
 // same time per slab). The dense MMA rate alone would give 2 x width; the
 // rest is time the MMA issuer waits for operands. Sharing A between two pairs
-// halves the A bytes each SM fetches from L2 but couples four CTAs' pipelines,
-// and measured slower per slab than the pair alone at this size.
+// halves the A bytes each SM fetches from L2 but measured no faster per slab
+// at this size, and its clusters of four leave a few SMs idle.
 constexpr double kSlabCycles[3][4] = {
     {672.0, 640.0, 605.0, 570.0},  // single CTA, 128 x width tiles
-    {567.0, 517.0, 498.0, 479.0},  // CTA pair, 256 x width tiles
-    {640.0, 565.0, 560.0, 540.0},  // two pairs sharing A, two 256 x width tiles
+    {564.0, 504.0, 499.0, 464.0},  // CTA pair, 256 x width tiles
+    {560.0, 503.0, 500.0, 470.0},  // two pairs sharing A, two 256 x width tiles
 };
 
 // Picks the kernel (single CTA, CTA pair, or two pairs sharing A), the tile
