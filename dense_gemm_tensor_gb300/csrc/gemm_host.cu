@@ -371,7 +371,8 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
 }
 
 int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-             void* C, int64_t ldc, int layout, void* stream_ptr, const ExternalScratch* ext = nullptr) {
+             void* C, int64_t ldc, int layout, void* stream_ptr, const ExternalScratch* ext = nullptr,
+             const gemm_epilogue_t* epi = nullptr) {
   const int es = (kind == KIND_TF32) ? 4 : 2;
   const int64_t kLim = (int64_t(1) << 31) - 1;
   if (M < 0 || N < 0 || K < 0 || M > kLim || N > kLim || K > kLim) return GEMM_ERR_INVALID_VALUE;
@@ -386,8 +387,14 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   if (ldc > (int64_t(1) << 40) / es) return GEMM_ERR_INVALID_VALUE;
   if (((M + 127) / 128) * ((N + 127) / 128) > kLim) return GEMM_ERR_INVALID_VALUE;
 
+  if (epi != nullptr && (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU_TANH))
+    return GEMM_ERR_INVALID_VALUE;
+  // the fused epilogue is on unless it is the identity
+  const bool fused = epi != nullptr && !(epi->alpha == 1.0f && epi->beta == 0.0f && epi->bias == nullptr &&
+                                         epi->activation == GEMM_ACT_NONE);
+  const void* bias = fused ? epi->bias : nullptr;
   auto mis = [es](const void* p) { return (reinterpret_cast<uintptr_t>(p) % es) != 0; };
-  if (mis(C) || (K > 0 && (mis(A) || mis(B)))) return GEMM_ERR_MISALIGNED;
+  if (mis(C) || (K > 0 && (mis(A) || mis(B))) || (bias != nullptr && mis(bias))) return GEMM_ERR_MISALIGNED;
 
   const DeviceInfo* dev = nullptr;
   int st = current_device(&dev);
@@ -396,10 +403,26 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   uintptr_t c0, c1;
   extent(C, M, N, ldc, es, &c0, &c1);
   if (!is_device_memory(C)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+  if (bias != nullptr) {
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(bias), s1 = s0 + uintptr_t(N) * es;
+    if (overlaps(c0, c1, s0, s1)) return GEMM_ERR_INVALID_VALUE;
+    if (!is_device_memory(bias)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+  }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   if (K == 0) {
-    cudaError_t e = launch_fill_zero(C, ldc, int(M), int(N), es, stream, dev->sm_count);
+    cudaError_t e;
+    if (fused) {
+      GemmParams ep;
+      memset(&ep, 0, sizeof(ep));
+      ep.alpha = epi->alpha;
+      ep.beta = epi->beta;
+      ep.bias = bias;
+      ep.act = epi->activation;
+      e = launch_epilogue_only(kind, C, ldc, int(M), int(N), ep, stream, dev->sm_count);
+    } else {
+      e = launch_fill_zero(C, ldc, int(M), int(N), es, stream, dev->sm_count);
+    }
     if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return GEMM_OK;
@@ -525,6 +548,13 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   p.epoch = ep;
   p.debug = g_debug_flags.load(std::memory_order_relaxed);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.fused = fused ? 1 : 0;
+  if (fused) {
+    p.alpha = epi->alpha;
+    p.beta = epi->beta;
+    p.bias = bias;
+    p.act = epi->activation;
+  }
 
   const CUtensorMapDataType dt = kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -591,6 +621,20 @@ int run_gemm_external(int kind, int64_t M, int64_t N, int64_t K, const void* A, 
   return run_gemm(kind, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, ext);
 }
 
+cudaError_t launch_epilogue_only(int kind, void* C, long long ldc, int M, int N, const GemmParams& p,
+                                 cudaStream_t stream, int sm_count) {
+  const long long total = static_cast<long long>(M) * N;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 4LL * sm_count) blocks = 4LL * sm_count;
+  if (kind == KIND_TF32)
+    epilogue_only_kernel<KIND_TF32><<<int(blocks), 256, 0, stream>>>(C, ldc, M, N, p.alpha, p.beta, p.bias, p.act);
+  else if (kind == KIND_BF16)
+    epilogue_only_kernel<KIND_BF16><<<int(blocks), 256, 0, stream>>>(C, ldc, M, N, p.alpha, p.beta, p.bias, p.act);
+  else
+    epilogue_only_kernel<KIND_F16><<<int(blocks), 256, 0, stream>>>(C, ldc, M, N, p.alpha, p.beta, p.bias, p.act);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count) {
   const long long total = static_cast<long long>(M) * N;
   long long blocks = (total + 255) / 256;
@@ -619,6 +663,21 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, co
 int gemm_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
               uint16_t* C, int64_t ldc, int layout, void* stream) {
   return dgt::run_gemm(dgt::KIND_BF16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream);
+}
+
+int gemm_tf32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
+                 int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream) {
+  return dgt::run_gemm(dgt::KIND_TF32, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue);
+}
+
+int gemm_f16_ex(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream) {
+  return dgt::run_gemm(dgt::KIND_F16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue);
+}
+
+int gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                 uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream) {
+  return dgt::run_gemm(dgt::KIND_BF16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue);
 }
 
 const char* gemm_status_string(int status) {

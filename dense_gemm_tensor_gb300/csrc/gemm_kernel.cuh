@@ -104,9 +104,16 @@ struct GemmParams {
   uint32_t epoch;    // unique per launch
   uint32_t debug;
   unsigned long long wait_limit_ns;
+  // Fused epilogue (fused != 0): C = act(alpha * A.B + beta * C + bias[col]),
+  // evaluated in fp32; beta == 0 leaves C unread; bias (N elements of the
+  // output type) may be null; act is a GEMM_ACT_* code.
+  int fused;
+  int act;
+  float alpha, beta;
+  const void* bias;
 };
 
-// Output staging in shared memory: 2 KB per epilogue warp (see epi_round).
+// Output staging in shared memory: 2 KB per epilogue warp (see epi_chunk_addr).
 constexpr int EPI_WARP_BYTES = 32 * 64;
 constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
 
@@ -305,7 +312,7 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
 // Each epilogue warp owns a 32-row x 64-byte tile of shared memory in the
 // layout of TMA's 64-byte swizzle: 16-byte chunk j of row r sits at
 // r * 64 + ((j ^ ((r >> 1) & 3)) * 16), so both the lanes' row writes (lane =
-// row) and the row-wise reads below are free of bank conflicts. One round
+// row) and the row-wise accesses below are free of bank conflicts. One round
 // stages 64 bytes of each of the warp's 32 rows -- 32 columns of a 16-bit C,
 // 16 of an fp32 C -- and writes them to C[row0 .., col0 ..]: by one TMA store
 // of the 32 x 64-byte box when C's base and row pitch are 16-byte multiples
@@ -318,14 +325,34 @@ __device__ __forceinline__ uint32_t epi_chunk_addr(uint32_t stage, int r, int j)
   return stage + static_cast<uint32_t>(r * 64) + (static_cast<uint32_t>(j ^ ((r >> 1) & 3)) << 4);
 }
 
-template <int KIND>
-__device__ __forceinline__ void epi_round(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage, int lane,
-                                          int row0, int col0, const uint32_t (&w)[16]) {
-  // the previous round's TMA store must have read the tile (only lane 0 has stores in flight)
+// The tile may be overwritten once the previous round's TMA store has read it
+// (only lane 0 has stores in flight).
+__device__ __forceinline__ void epi_acquire(const GemmParams& p, int lane) {
   if (p.c_tma && lane == 0) bulk_wait_read_all();
   __syncwarp();
+}
+
+__device__ __forceinline__ void epi_put_row(uint32_t stage, int lane, const uint32_t (&w)[16]) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) st_shared_v4(epi_chunk_addr(stage, lane, j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  for (int j = 0; j < 4; ++j)
+    st_shared_v4(epi_chunk_addr(stage, lane, j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
+__device__ __forceinline__ void epi_get_row(uint32_t stage, int lane, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t a = epi_chunk_addr(stage, lane, j);
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4 * j]), "=r"(w[4 * j + 1]), "=r"(w[4 * j + 2]), "=r"(w[4 * j + 3])
+                 : "r"(a)
+                 : "memory");
+  }
+}
+
+// Writes the staged tile to C[row0 .., col0 ..] (see above).
+template <int KIND>
+__device__ __forceinline__ void epi_flush(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage, int lane,
+                                          int row0, int col0) {
   constexpr int ROUND_COLS = KIND == KIND_TF32 ? 16 : 32;
   if (p.c_tma && col0 + ROUND_COLS <= p.N) {
     fence_proxy_async_smem();  // make the tile visible to the TMA unit
@@ -358,12 +385,117 @@ __device__ __forceinline__ void epi_round(const GemmParams& p, const CUtensorMap
   }
 }
 
+// Loads C's current 32 x 64-byte block at (row0, col0) into the tile with
+// coalesced loads (the mirror of the row-wise stores); zeros outside M x N.
+template <int KIND>
+__device__ __forceinline__ void epi_load_c(const GemmParams& p, uint32_t stage, int lane, int row0, int col0) {
+  constexpr int ES = KIND == KIND_TF32 ? 4 : 2;
+  const int l = lane & 15;
+  const int col = col0 + l * (4 / ES);
+#pragma unroll 4
+  for (int rr = 0; rr < 32; rr += 2) {
+    const int r = rr + (lane >> 4);
+    const int row = row0 + r;
+    uint32_t v = 0;
+    if (row < p.M && col < p.N) {
+      const uint8_t* src =
+          reinterpret_cast<const uint8_t*>(p.C) + (static_cast<long long>(row) * p.ldc + col) * ES;
+      if (ES == 4 || (p.c_gran >= 4 && col + 1 < p.N)) {
+        v = *reinterpret_cast<const uint32_t*>(src);
+      } else {
+        v = reinterpret_cast<const uint16_t*>(src)[0];
+        if (col + 1 < p.N) v |= static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(src)[1]) << 16;
+      }
+    }
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(epi_chunk_addr(stage, r, l >> 2) + ((l & 3) << 2)), "r"(v)
+                 : "memory");
+  }
+  __syncwarp();
+}
+
+// Element k (0 .. 64 / ES - 1) of a staged row, as float.
+template <int KIND>
+__device__ __forceinline__ float epi_elem(const uint32_t (&w)[16], int k) {
+  if constexpr (KIND == KIND_TF32) {
+    return __uint_as_float(w[k]);
+  } else {
+    const uint32_t h = (k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu);
+    if constexpr (KIND == KIND_BF16)
+      return __uint_as_float(h << 16);
+    else
+      return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+  }
+}
+
+// Activation of the fused epilogue (GEMM_ACT_* of the C interface).
+__device__ __forceinline__ float epi_activation(float v, int act) {
+  if (act == 1) return v < 0.0f ? 0.0f : v;                                   // ReLU
+  if (act == 2) return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));   // GELU, x * Phi(x)
+  if (act == 3) {                                                             // GELU, tanh form
+    const float u = 0.79788456080286536f * (v + 0.044715f * v * v * v);
+    return 0.5f * v * (1.0f + tanhf(u));
+  }
+  return v;
+}
+
+// One round with the fused epilogue: out = act(alpha * acc + beta * C + bias[col]),
+// in fp32, then rounded to the output type. The round's accumulator columns
+// are r[OFF .. OFF + 63 / ES] (32 for 16-bit C, 16 for fp32 C).
+template <int KIND, int OFF>
+__device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage,
+                                                int lane, int row0, int col0, const uint32_t (&r)[32]) {
+  constexpr int RC = KIND == KIND_TF32 ? 16 : 32;
+  using T = typename KindTraits<KIND>::T;
+  epi_acquire(p, lane);
+  float v[RC];
+#pragma unroll
+  for (int k = 0; k < RC; ++k) v[k] = p.alpha * __uint_as_float(r[OFF + k]);
+  if (p.beta != 0.0f) {
+    epi_load_c<KIND>(p, stage, lane, row0, col0);
+    uint32_t w[16];
+    epi_get_row(stage, lane, w);
+#pragma unroll
+    for (int k = 0; k < RC; ++k) v[k] += p.beta * epi_elem<KIND>(w, k);
+    __syncwarp();  // every lane has read its row before the tile is overwritten
+  }
+  if (p.bias != nullptr) {
+    const T* bias = static_cast<const T*>(p.bias);
+#pragma unroll
+    for (int k = 0; k < RC; ++k)
+      if (col0 + k < p.N) {
+        if constexpr (KIND == KIND_TF32)
+          v[k] += bias[col0 + k];
+        else if constexpr (KIND == KIND_BF16)
+          v[k] += __bfloat162float(bias[col0 + k]);
+        else
+          v[k] += __half2float(bias[col0 + k]);
+      }
+  }
+  uint32_t w[16];
+  if constexpr (KIND == KIND_TF32) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) w[k] = __float_as_uint(epi_activation(v[k], p.act));
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      w[k] = pack2<KIND>(__float_as_uint(epi_activation(v[2 * k], p.act)),
+                         __float_as_uint(epi_activation(v[2 * k + 1], p.act)));
+  }
+  epi_put_row(stage, lane, w);
+  epi_flush<KIND>(p, tmC, stage, lane, row0, col0);
+}
+
 // Converts 32 accumulator columns of the warp's 32 rows (lane = row, values
-// in r) to the output type and writes them to C[row0 .., col0 .. col0+31].
-// Warp-collective.
+// in r) to the output type and writes them to C[row0 .., col0 .. col0+31],
+// through the fused epilogue when the launch has one. Warp-collective.
 template <int KIND>
 __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage, int lane,
                                            int row0, int col0, const uint32_t (&r)[32]) {
+  if (p.fused) {
+    epi_round_fused<KIND, 0>(p, tmC, stage, lane, row0, col0, r);
+    if (KIND == KIND_TF32 && col0 + 16 < p.N) epi_round_fused<KIND, 16>(p, tmC, stage, lane, row0, col0 + 16, r);
+    return;
+  }
   if constexpr (KIND == KIND_TF32) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -371,13 +503,17 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
       uint32_t w[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) w[j] = r[16 * h + j];
-      epi_round<KIND>(p, tmC, stage, lane, row0, col0 + 16 * h, w);
+      epi_acquire(p, lane);
+      epi_put_row(stage, lane, w);
+      epi_flush<KIND>(p, tmC, stage, lane, row0, col0 + 16 * h);
     }
   } else {
     uint32_t w[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) w[j] = pack2<KIND>(r[2 * j], r[2 * j + 1]);
-    epi_round<KIND>(p, tmC, stage, lane, row0, col0, w);
+    epi_acquire(p, lane);
+    epi_put_row(stage, lane, w);
+    epi_flush<KIND>(p, tmC, stage, lane, row0, col0);
   }
 }
 
@@ -641,6 +777,36 @@ __global__ void fill_zero_kernel(void* C, long long ldc, int M, int N) {
       reinterpret_cast<uint32_t*>(C)[r * ldc + c] = 0u;
     else
       reinterpret_cast<uint16_t*>(C)[r * ldc + c] = 0;
+  }
+}
+
+// K = 0 with the fused epilogue: C = act(alpha * 0 + beta * C + bias[col]),
+// in fp32, rounded to the output type.
+template <int KIND>
+__global__ void epilogue_only_kernel(void* C, long long ldc, int M, int N, float alpha, float beta,
+                                     const void* bias, int act) {
+  using T = typename KindTraits<KIND>::T;
+  const long long total = static_cast<long long>(M) * N;
+  T* c = static_cast<T*>(C);
+  const T* b = static_cast<const T*>(bias);
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / N, col = i - r * N;
+    T* e = c + r * ldc + col;
+    float v = alpha * 0.0f;
+    if constexpr (KIND == KIND_TF32) {
+      if (beta != 0.0f) v += beta * *e;
+      if (b != nullptr) v += b[col];
+      *e = epi_activation(v, act);
+    } else if constexpr (KIND == KIND_BF16) {
+      if (beta != 0.0f) v += beta * __bfloat162float(*e);
+      if (b != nullptr) v += __bfloat162float(b[col]);
+      *e = __float2bfloat16_rn(epi_activation(v, act));
+    } else {
+      if (beta != 0.0f) v += beta * __half2float(*e);
+      if (b != nullptr) v += __half2float(b[col]);
+      *e = __float2half_rn(epi_activation(v, act));
+    }
   }
 }
 

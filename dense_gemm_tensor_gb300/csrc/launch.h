@@ -30,6 +30,9 @@ int pair_clusters_f16(bool kmajor, int bn, int pairs);
 int pair_clusters_bf16(bool kmajor, int bn, int pairs);
 int pair_clusters_tf32(bool kmajor, int bn, int pairs);
 cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count);
+// The K = 0 product with a fused epilogue (epilogue_only_kernel).
+cudaError_t launch_epilogue_only(int kind, void* C, long long ldc, int M, int N, const GemmParams& p,
+                                 cudaStream_t stream, int sm_count);
 // Copies rows of `row_bytes` from a source with `gran`-byte-aligned row starts
 // to a destination with 16-byte-aligned rows (pack_rows_kernel).
 cudaError_t launch_pack(const void* src, int64_t src_ld_bytes, void* dst, int64_t dst_ld_bytes, int64_t rows,

@@ -31,10 +31,24 @@ GEMM_ERR_DRIVER = 6
 GEMM_ERR_DEVICE_TIMEOUT = 7
 GEMM_ERR_SCRATCH_LIMIT = 8
 
+GEMM_ACT_NONE = 0
+GEMM_ACT_RELU = 1
+GEMM_ACT_GELU = 2
+GEMM_ACT_GELU_TANH = 3
+ACTIVATIONS = {None: GEMM_ACT_NONE, "none": GEMM_ACT_NONE, "relu": GEMM_ACT_RELU, "gelu": GEMM_ACT_GELU,
+               "gelu_tanh": GEMM_ACT_GELU_TANH}
+
+
+class Epilogue(ctypes.Structure):
+    """gemm_epilogue_t: C = act(alpha * A.B + beta * C + bias[col])."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("activation", ctypes.c_int)]
+
 # Every symbol the C header declares.
-EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_get_device_status",
-           "gemm_reset_device_status", "gemm_set_debug", "gemm_launch_count", "gemm_set_tuning",
-           "gemm_last_plan", "gemm_free_workspaces", "gemm_bf16_static_scratch")
+EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_tf32_ex", "gemm_f16_ex", "gemm_bf16_ex",
+           "gemm_status_string", "gemm_get_device_status", "gemm_reset_device_status", "gemm_set_debug",
+           "gemm_launch_count", "gemm_set_tuning", "gemm_last_plan", "gemm_free_workspaces",
+           "gemm_bf16_static_scratch")
 
 _lib = None
 
@@ -58,6 +72,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     for name in ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_bf16_static_scratch"):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, vp]
+        fn.restype = ctypes.c_int
+    for name in ("gemm_tf32_ex", "gemm_f16_ex", "gemm_bf16_ex"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, ctypes.POINTER(Epilogue), vp]
         fn.restype = ctypes.c_int
     lib.gemm_status_string.argtypes = [ctypes.c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
@@ -108,8 +126,17 @@ def gemm_bf16_static_scratch(M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_
     return _call("gemm_bf16_static_scratch", M, N, K, A, lda, B, ldb, C, ldc, layout, stream)
 
 
+def gemm_ex(dtype_name, M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_MAJOR, epilogue=None,
+            stream=None) -> int:
+    """gemm_{tf32,f16,bf16}_ex with raw device pointers; `epilogue` an Epilogue or None."""
+    fn = getattr(load(), f"gemm_{dtype_name}_ex")
+    return fn(M, N, K, A, lda, B, ldb, C, ldc, layout, ctypes.byref(epilogue) if epilogue is not None else None,
+              stream)
+
+
 _BY_DTYPE = {torch.float32: "gemm_tf32", torch.float16: "gemm_f16", torch.bfloat16: "gemm_bf16"}
 _FN = {}  # dtype -> bound C function, filled on first use
+_FN_EX = {}
 
 
 def _rows(t: torch.Tensor, what: str) -> int:
@@ -124,14 +151,19 @@ def _rows(t: torch.Tensor, what: str) -> int:
 
 
 def matmul(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, layout: int = GEMM_B_ROW_MAJOR,
-           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """C = A . B on the current CUDA device.
+           stream: torch.cuda.Stream | None = None, alpha: float = 1.0, beta: float = 0.0,
+           bias: torch.Tensor | None = None, activation: str | None = None) -> torch.Tensor:
+    """C = A . B on the current CUDA device, or with a fused epilogue
+    C = act(alpha * A . B + beta * C + bias) when any of alpha, beta, bias,
+    activation ("relu", "gelu", "gelu_tanh") differs from the identity.
 
     ``A``: M x K. ``B``: K x N for ``layout=GEMM_B_ROW_MAJOR``, or N x K (B
     transposed) for ``layout=GEMM_B_K_MAJOR``. Rows may be padded (stride(0) >
     row length) but elements along a row must be contiguous. The dtype selects
     the entry point: float32 -> gemm_tf32, float16 -> gemm_f16, bfloat16 ->
-    gemm_bf16. ``out`` (M x N, same dtype) may have padded rows too.
+    gemm_bf16 (the *_ex variants with an epilogue). ``out`` (M x N, same dtype)
+    may have padded rows too; with beta != 0 it supplies the C that is scaled
+    and added. ``bias``: N elements of the same dtype, contiguous.
     """
     dt = A.dtype
     fn = _FN.get(dt)
@@ -157,10 +189,27 @@ def matmul(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *,
     elif out.dtype != dt or tuple(out.shape) != (M, N):
         raise ValueError("out must be M x N with the operands' dtype")
     s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
-    code = fn(M, N, K, A.data_ptr() or None, _rows(A, "A"), B.data_ptr() or None, _rows(B, "B"),
-              out.data_ptr() or None, _rows(out, "out"), layout, s)
+    if alpha == 1.0 and beta == 0.0 and bias is None and activation is None:
+        code = fn(M, N, K, A.data_ptr() or None, _rows(A, "A"), B.data_ptr() or None, _rows(B, "B"),
+                  out.data_ptr() or None, _rows(out, "out"), layout, s)
+        if code != GEMM_OK:
+            raise GemmError(code, _BY_DTYPE[dt])
+        return out
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(k for k in ACTIVATIONS if k)}")
+    if bias is not None:
+        if bias.dtype != dt or bias.dim() != 1 or bias.numel() != N or not bias.is_cuda or \
+                (N > 1 and bias.stride(0) != 1):
+            raise ValueError("bias must be a contiguous CUDA vector of N elements of the operands' dtype")
+    fx = _FN_EX.get(dt)
+    if fx is None:
+        fx = _FN_EX[dt] = getattr(load(), _BY_DTYPE[dt] + "_ex")
+    epi = Epilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None,
+                   ACTIVATIONS[activation])
+    code = fx(M, N, K, A.data_ptr() or None, _rows(A, "A"), B.data_ptr() or None, _rows(B, "B"),
+              out.data_ptr() or None, _rows(out, "out"), layout, ctypes.byref(epi), s)
     if code != GEMM_OK:
-        raise GemmError(code, _BY_DTYPE[dt])
+        raise GemmError(code, _BY_DTYPE[dt] + "_ex")
     return out
 
 

@@ -55,9 +55,18 @@
  * Any base address and leading dimension that keeps elements aligned to
  * their size is accepted. Rows whose byte pitch is a multiple of 16 (and 16-byte
  * aligned bases) are streamed with TMA; another A or B is first packed into
- * 16-byte-aligned rows in the stream's scratch buffer (one bandwidth-bound
+ * 128-byte-aligned rows in the stream's scratch buffer (one bandwidth-bound
  * copy kernel), and if no scratch can be had it is read in place by the
- * kernel's copy warps, which is slower but gives the same results.
+ * kernel's copy warps, which is slower but gives the same results. In large
+ * products an A or B whose rows are 16- but not 128-byte aligned is packed too
+ * (it streams faster that way).
+ *
+ * Fused epilogue (gemm_*_ex): the same product followed, per element, by
+ *   C[i][j] = act(alpha * (A.B)[i][j] + beta * C[i][j] + bias[j])
+ * evaluated in fp32 from the fp32 accumulator, then rounded once to the
+ * output type (RNE). This is the usual GEMM epilogue of BLAS-style libraries
+ * (scales, a per-column bias, an activation); the GEMM pages' kernels stop at
+ * C = A . B, so these calls go beyond them.
  */
 #ifndef DGT_GEMM_H
 #define DGT_GEMM_H
@@ -85,6 +94,27 @@ extern "C" {
 
 /* Limits: M, N, K < 2^31; the number of 128 x 128 output tiles < 2^31. */
 
+/* Activations of the fused epilogue */
+#define GEMM_ACT_NONE 0
+#define GEMM_ACT_RELU 1      /* max(x, 0); NaN stays NaN */
+#define GEMM_ACT_GELU 2      /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)) */
+#define GEMM_ACT_GELU_TANH 3 /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+
+/*
+ * Fused-epilogue parameters. alpha scales the product, beta the current C
+ * (beta == 0: C is only written, never read, so it may hold anything,
+ * including NaN); bias is NULL or N elements of the output type on the
+ * current device (element j is added to column j), and must not overlap C;
+ * activation is a GEMM_ACT_* code. alpha = 1, beta = 0, bias = NULL,
+ * activation = GEMM_ACT_NONE gives exactly the plain call's result.
+ */
+typedef struct gemm_epilogue {
+  float alpha;
+  float beta;
+  const void* bias;
+  int activation;
+} gemm_epilogue_t;
+
 /* C = A . B with TF32 tensor-core inputs; A, B, C fp32. */
 int gemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
               int64_t ldc, int layout, void* stream);
@@ -96,6 +126,22 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, co
 /* C = A . B with bfloat16 inputs and output (uint16_t bit patterns). */
 int gemm_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
               uint16_t* C, int64_t ldc, int layout, void* stream);
+
+/*
+ * The three products with the fused epilogue described at the top of this
+ * file. `epilogue` NULL is the plain call. Beyond the plain call's checks:
+ * GEMM_ERR_INVALID_VALUE for an activation code outside GEMM_ACT_*, or a bias
+ * that overlaps C; GEMM_ERR_MISALIGNED for a bias not aligned to its element
+ * size; GEMM_ERR_NOT_DEVICE_MEMORY for a bias that is not device memory. With
+ * beta != 0 each element of C is read once, before it is written, by the same
+ * thread; with K = 0 the result is act(beta * C + bias).
+ */
+int gemm_tf32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
+                 int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream);
+int gemm_f16_ex(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream);
+int gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                 uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream);
 
 /*
  * gemm_bf16_static_scratch: gemm_bf16 for callers that cannot allocate.
@@ -113,7 +159,7 @@ int gemm_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, c
  * 256 KiB, plus their counters). A shape whose plan needs more is refused with
  * GEMM_ERR_SCRATCH_LIMIT and nothing is launched; shapes that split nothing
  * use no scratch at all. Every GPU that loads the library keeps the array
- * (16 MiB + 16 KiB) until the process exits.
+ * (16 MiB + 32 KiB) until the process exits.
  *
  * The first call on each device, with that device current, looks up the
  * array's device address and zeroes its counters (a short synchronous step);
