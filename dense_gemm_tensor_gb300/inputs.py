@@ -30,6 +30,8 @@ DTYPES = {
     "bf16": torch.bfloat16,
     "f16": torch.float16,
     "tf32": torch.float32,
+    "e4m3": torch.float8_e4m3fn,  # OCP FP8 bytes; the FP8 products write a bfloat16 C
+    "e5m2": torch.float8_e5m2,
 }
 
 
