@@ -69,7 +69,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, _sources()))
     tmp = LIB + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]

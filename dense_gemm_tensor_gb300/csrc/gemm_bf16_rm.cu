@@ -1,0 +1,5 @@
+// BF16, row-major B: every GEMM kernel instantiation of this operand kind and layout.
+#include "launch.h"
+namespace dgt {
+DGT_DEFINE_VARIANTS(bf16_rm, KIND_BF16, false)
+}  // namespace dgt

@@ -20,7 +20,7 @@ namespace dgt {
 __device__ uint32_t g_status_words[2];
 
 // Copies a rows x row_bytes matrix from a source whose row starts are only
-// `gran`-byte aligned (gran in {2, 4, 8, 16}) to a destination with 16-byte
+// `gran`-byte aligned (gran in {1, 2, 4, 8, 16}) to a destination with 16-byte
 // aligned rows of dst_ld_bytes. Each thread moves one 16-byte destination
 // chunk (consecutive threads take consecutive chunks of a row, so reads and
 // writes coalesce); bytes of the last chunk beyond row_bytes are zero.
@@ -46,24 +46,49 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint8_t* __restric
       } else if (gran == 4) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) w[q] = reinterpret_cast<const uint32_t*>(s)[q];
-      } else {
+      } else if (gran == 2) {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           w[q] = uint32_t(reinterpret_cast<const uint16_t*>(s)[2 * q]) |
                  (uint32_t(reinterpret_cast<const uint16_t*>(s)[2 * q + 1]) << 16);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) w[q >> 2] |= uint32_t(s[q]) << (8 * (q & 3));
       }
     } else {
-      // ragged end of the row: 2-byte pieces (every element size here is a multiple of 2)
-      uint16_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int q = 0; q < 8; ++q)
-        if (2 * q < valid) h[q] = reinterpret_cast<const uint16_t*>(s)[q];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) w[q] = uint32_t(h[2 * q]) | (uint32_t(h[2 * q + 1]) << 16);
+      // ragged end of the row: byte by byte
+      for (int q = 0; q < 16; ++q)
+        if (q < valid) w[q >> 2] |= uint32_t(s[q]) << (8 * (q & 3));
     }
     *reinterpret_cast<uint4*>(dst + r * dst_ld_bytes + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
+// dst[n][k] = src[k][n] for a rows x cols byte matrix (rows = K, cols = N):
+// a row-major K x N FP8 B becomes the K-major N x K operand the FP8 kernels
+// read. 32 x 32 tiles through shared memory (reads along src rows, writes
+// along dst rows); the tiles are strided over the grid.
+__global__ void __launch_bounds__(256) transpose_bytes_kernel(const uint8_t* __restrict__ src, long long src_ld,
+                                                              uint8_t* __restrict__ dst, long long dst_ld,
+                                                              int rows, int cols) {
+  __shared__ uint8_t tile[32][33];
+  const int tiles_c = (cols + 31) / 32;
+  const long long ntiles = static_cast<long long>((rows + 31) / 32) * tiles_c;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int r0 = static_cast<int>(t / tiles_c) * 32, c0 = static_cast<int>(t % tiles_c) * 32;
+    for (int i = ty; i < 32; i += 8) {
+      const int r = r0 + i, c = c0 + tx;
+      tile[i][tx] = (r < rows && c < cols) ? src[static_cast<long long>(r) * src_ld + c] : uint8_t(0);
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+      const int c = c0 + i, r = r0 + tx;  // dst row c, column r
+      if (c < cols && r < rows) dst[static_cast<long long>(c) * dst_ld + r] = tile[tx][i];
+    }
+    __syncthreads();
+  }
+}
 
 namespace {
 
@@ -182,7 +207,7 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 }
 
 // Co-resident CTA pairs of each pair-kernel variant, per device (-1 = not queried yet).
-std::atomic<int> g_pair_clusters[kMaxDevices][3][2][4][2];
+std::atomic<int> g_pair_clusters[kMaxDevices][5][2][4][2];
 std::once_flag g_pair_once;
 
 int pair_clusters(int dev, int kind, bool kmajor, int bn, int pairs) {
@@ -197,9 +222,14 @@ int pair_clusters(int dev, int kind, bool kmajor, int bn, int pairs) {
   std::atomic<int>& slot = g_pair_clusters[dev][kind][kmajor ? 1 : 0][wi][pairs - 1];
   int n = slot.load(std::memory_order_acquire);
   if (n < 0) {
-    n = kind == KIND_TF32 ? pair_clusters_tf32(kmajor, bn, pairs)
-        : kind == KIND_BF16 ? pair_clusters_bf16(kmajor, bn, pairs)
-                            : pair_clusters_f16(kmajor, bn, pairs);
+    switch (kind) {
+      case KIND_TF32: n = kmajor ? pair_clusters_tf32_km(bn, pairs) : pair_clusters_tf32_rm(bn, pairs); break;
+      case KIND_BF16: n = kmajor ? pair_clusters_bf16_km(bn, pairs) : pair_clusters_bf16_rm(bn, pairs); break;
+      case KIND_F16: n = kmajor ? pair_clusters_f16_km(bn, pairs) : pair_clusters_f16_rm(bn, pairs); break;
+      case KIND_E4M3: n = kmajor ? pair_clusters_e4m3_km(bn, pairs) : 0; break;
+      case KIND_E5M2: n = kmajor ? pair_clusters_e5m2_km(bn, pairs) : 0; break;
+      default: n = 0;
+    }
     slot.store(n, std::memory_order_release);
   }
   return n;
@@ -373,7 +403,10 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
 int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
              void* C, int64_t ldc, int layout, void* stream_ptr, const ExternalScratch* ext = nullptr,
              const gemm_epilogue_t* epi = nullptr) {
-  const int es = (kind == KIND_TF32) ? 4 : 2;
+  const bool fp8 = kind == KIND_E4M3 || kind == KIND_E5M2;
+  const int es = (kind == KIND_TF32) ? 4 : fp8 ? 1 : 2;  // operand element size
+  const int eo = (kind == KIND_TF32) ? 4 : 2;             // output element size (FP8 writes bfloat16)
+  const int out_kind = fp8 ? int(KIND_BF16) : kind;
   const int64_t kLim = (int64_t(1) << 31) - 1;
   if (M < 0 || N < 0 || K < 0 || M > kLim || N > kLim || K > kLim) return GEMM_ERR_INVALID_VALUE;
   if (layout != GEMM_B_ROW_MAJOR && layout != GEMM_B_K_MAJOR) return GEMM_ERR_INVALID_VALUE;
@@ -384,7 +417,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     if (ldb < (layout == GEMM_B_ROW_MAJOR ? N : K)) return GEMM_ERR_INVALID_VALUE;
     if (lda > (int64_t(1) << 40) / es || ldb > (int64_t(1) << 40) / es) return GEMM_ERR_INVALID_VALUE;
   }
-  if (ldc > (int64_t(1) << 40) / es) return GEMM_ERR_INVALID_VALUE;
+  if (ldc > (int64_t(1) << 40) / eo) return GEMM_ERR_INVALID_VALUE;
   if (((M + 127) / 128) * ((N + 127) / 128) > kLim) return GEMM_ERR_INVALID_VALUE;
 
   if (epi != nullptr && (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU_TANH))
@@ -393,18 +426,19 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   const bool fused = epi != nullptr && !(epi->alpha == 1.0f && epi->beta == 0.0f && epi->bias == nullptr &&
                                          epi->activation == GEMM_ACT_NONE);
   const void* bias = fused ? epi->bias : nullptr;
-  auto mis = [es](const void* p) { return (reinterpret_cast<uintptr_t>(p) % es) != 0; };
-  if (mis(C) || (K > 0 && (mis(A) || mis(B))) || (bias != nullptr && mis(bias))) return GEMM_ERR_MISALIGNED;
+  auto mis = [](const void* p, int size) { return (reinterpret_cast<uintptr_t>(p) % size) != 0; };
+  if (mis(C, eo) || (K > 0 && (mis(A, es) || mis(B, es))) || (bias != nullptr && mis(bias, eo)))
+    return GEMM_ERR_MISALIGNED;
 
   const DeviceInfo* dev = nullptr;
   int st = current_device(&dev);
   if (st != GEMM_OK) return st;
 
   uintptr_t c0, c1;
-  extent(C, M, N, ldc, es, &c0, &c1);
+  extent(C, M, N, ldc, eo, &c0, &c1);
   if (!is_device_memory(C)) return GEMM_ERR_NOT_DEVICE_MEMORY;
   if (bias != nullptr) {
-    const uintptr_t s0 = reinterpret_cast<uintptr_t>(bias), s1 = s0 + uintptr_t(N) * es;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(bias), s1 = s0 + uintptr_t(N) * eo;
     if (overlaps(c0, c1, s0, s1)) return GEMM_ERR_INVALID_VALUE;
     if (!is_device_memory(bias)) return GEMM_ERR_NOT_DEVICE_MEMORY;
   }
@@ -419,9 +453,9 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
       ep.beta = epi->beta;
       ep.bias = bias;
       ep.act = epi->activation;
-      e = launch_epilogue_only(kind, C, ldc, int(M), int(N), ep, stream, dev->sm_count);
+      e = launch_epilogue_only(out_kind, C, ldc, int(M), int(N), ep, stream, dev->sm_count);
     } else {
-      e = launch_fill_zero(C, ldc, int(M), int(N), es, stream, dev->sm_count);
+      e = launch_fill_zero(C, ldc, int(M), int(N), eo, stream, dev->sm_count);
     }
     if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -441,7 +475,10 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   memset(&L, 0, sizeof(L));
   GemmParams& p = L.p;
   int ga = granularity(A, lda, es), gb = granularity(B, ldb, es);
-  const bool kmajor = layout == GEMM_B_K_MAJOR;
+  // The FP8 kernels read B K-major only: a row-major FP8 B is transposed into
+  // the stream's scratch first (the packed-B slot), and from then on it is K-major.
+  const bool transpose_b = fp8 && layout == GEMM_B_ROW_MAJOR;
+  const bool kmajor = layout == GEMM_B_K_MAJOR || transpose_b;
   int dev_id = 0;
   cudaGetDevice(&dev_id);
   // Operands whose rows TMA cannot address (row starts not 16-byte aligned)
@@ -452,18 +489,21 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   // boundaries: each 128-byte row of its boxes then straddles two L2 lines,
   // and the k-loop ran about a third slower (4000 x 4100 x 4104 on GB300). The
   // copy pays for itself once the other output dimension is a few thousand.
-  const bool may_pack = ext == nullptr && !(g_debug_flags.load(std::memory_order_relaxed) & DEBUG_NO_PACK);
+  // FP8 operands always go through TMA (the copy warps do not handle 1-byte
+  // granules), so they are packed whenever they need it.
+  const bool may_pack =
+      ext == nullptr && (fp8 || !(g_debug_flags.load(std::memory_order_relaxed) & DEBUG_NO_PACK));
   auto off_line = [es](const void* ptr, int64_t ld) {
     return ((reinterpret_cast<uintptr_t>(ptr) | static_cast<uintptr_t>(ld * es)) % 128) != 0;
   };
   const bool big = 2.0 * double(M) * double(N) * double(K) >= 1.6e10;
   const bool pack_a = may_pack && (ga < 16 || (big && N >= 2048 && off_line(A, lda)));
-  const bool pack_b = may_pack && (gb < 16 || (big && M >= 2048 && off_line(B, ldb)));
+  const bool pack_b = may_pack && (transpose_b || gb < 16 || (big && M >= 2048 && off_line(B, ldb)));
   TilePlan plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, (ga == 16 || pack_a) && (gb == 16 || pack_b),
                               dev->sm_count);
   // Scratch for this plan, laid out as [counters][split partials][packed A][packed B].
   const int64_t lda_p = pack_a ? (K * es + 127) / 128 * 128 / es : lda;
-  const int64_t b_rows = kmajor ? N : K, b_cols = kmajor ? K : N;
+  const int64_t b_rows = kmajor ? N : K, b_cols = kmajor ? K : N;  // of the operand the kernel reads
   const int64_t ldb_p = pack_b ? (b_cols * es + 127) / 128 * 128 / es : ldb;
   auto split_tiles = [&](const TilePlan& pl) {
     const int64_t tm = (M + (pl.pair ? 255 : 127)) / (pl.pair ? 256 : 128);
@@ -486,6 +526,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     ws = static_cast<char*>(stream_workspace(dev_id, stream, total < kCounterBytes ? kCounterBytes : total));
     if (ws == nullptr) {
       // no scratch: no split tail, and unaligned operands are read in place by the copy warps
+      if (fp8 && (pack_a || pack_b)) return GEMM_ERR_LAUNCH;  // FP8 cannot do without the packed copy
       if (pack_a || pack_b) plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, ga == 16 && gb == 16, dev->sm_count);
       rest = 0;
     }
@@ -521,9 +562,13 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     ga = 16;
   }
   if (pack_b && ws != nullptr) {
-    if (launch_pack(B, ldb * es, ws + off_b, ldb_p * es, b_rows, b_cols * es, gb, stream, dev->sm_count) !=
-        cudaSuccess)
+    if (transpose_b) {
+      if (launch_transpose_bytes(B, ldb, ws + off_b, ldb_p, K, N, stream, dev->sm_count) != cudaSuccess)
+        return GEMM_ERR_LAUNCH;
+    } else if (launch_pack(B, ldb * es, ws + off_b, ldb_p * es, b_rows, b_cols * es, gb, stream, dev->sm_count) !=
+               cudaSuccess) {
       return GEMM_ERR_LAUNCH;
+    }
     B = ws + off_b;
     ldb = ldb_p;
     gb = 16;
@@ -540,7 +585,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   p.copy_bytes = 16;
   if (!p.a_tma) p.copy_bytes = ga;
   if (!p.b_tma && gb < p.copy_bytes) p.copy_bytes = gb;
-  p.c_gran = granularity(C, ldc, es);
+  p.c_gran = granularity(C, ldc, eo);
   p.c_tma = p.c_gran == 16;
   p.status = dev->status_words;
   uint32_t ep = g_epoch.fetch_add(1, std::memory_order_relaxed);
@@ -558,7 +603,9 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
 
   const CUtensorMapDataType dt = kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+                                 : kind == KIND_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType dt_out = fp8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : dt;
   const uint32_t bk = 128 / es;  // K elements per 128-byte row
   // A box: 128 rows, or 64 where two pairs each load half a CTA's rows for both
   if (p.a_tma && !encode_2d(&L.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda) * es, bk,
@@ -566,7 +613,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     return GEMM_ERR_DRIVER;
   if (p.b_tma) {
     bool ok;
-    if (layout == GEMM_B_K_MAJOR) {
+    if (kmajor) {
       ok = encode_2d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, bk,
                      uint32_t(plan.pair ? bn / 2 : bn));
     } else {
@@ -576,7 +623,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     if (!ok) return GEMM_ERR_DRIVER;
   }
   // C box: 32 rows x 64 bytes, the staging tile of one epilogue warp (64-byte swizzle)
-  if (p.c_tma && !encode_2d(&L.tmC, dt, C, uint64_t(N), uint64_t(M), uint64_t(ldc) * es, uint32_t(64 / es), 32,
+  if (p.c_tma && !encode_2d(&L.tmC, dt_out, C, uint64_t(N), uint64_t(M), uint64_t(ldc) * eo, uint32_t(64 / eo), 32,
                             CU_TENSOR_MAP_SWIZZLE_64B))
     return GEMM_ERR_DRIVER;
   L.b_kmajor = kmajor;
@@ -592,7 +639,15 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
       p.tail_segs > kMaxTailSegs || L.grid < 1 || (L.pair && (L.grid % (2 * L.pairs) != 0)) || p.tiles_n < 1 ||
       p.tiles_m < 1 || (L.pair && L.pairs != 1 && L.pairs != 2) || (!L.pair && L.pairs != 1))
     return GEMM_ERR_LAUNCH;
-  cudaError_t e = kind == KIND_TF32 ? launch_tf32(L) : kind == KIND_BF16 ? launch_bf16(L) : launch_f16(L);
+  if (fp8 && !(p.a_tma && p.b_tma && kmajor)) return GEMM_ERR_LAUNCH;  // guaranteed by the packing above
+  cudaError_t e;
+  switch (kind) {
+    case KIND_TF32: e = kmajor ? launch_tf32_km(L) : launch_tf32_rm(L); break;
+    case KIND_BF16: e = kmajor ? launch_bf16_km(L) : launch_bf16_rm(L); break;
+    case KIND_F16: e = kmajor ? launch_f16_km(L) : launch_f16_rm(L); break;
+    case KIND_E4M3: e = launch_e4m3_km(L); break;
+    default: e = launch_e5m2_km(L); break;
+  }
   if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   const int32_t info[8] = {plan.pair ? 2 * plan.pairs : 1, bn, p.raster, L.grid, p.tail_segs, plan.conc, p.tail_start,
@@ -635,6 +690,17 @@ cudaError_t launch_epilogue_only(int kind, void* C, long long ldc, int M, int N,
   return cudaGetLastError();
 }
 
+cudaError_t launch_transpose_bytes(const void* src, int64_t src_ld, void* dst, int64_t dst_ld, int64_t rows,
+                                   int64_t cols, cudaStream_t stream, int sm_count) {
+  const long long tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
+  long long blocks = tiles < 16LL * sm_count ? tiles : 16LL * sm_count;
+  transpose_bytes_kernel<<<int(blocks), 256, 0, stream>>>(static_cast<const uint8_t*>(src), src_ld,
+                                                          static_cast<uint8_t*>(dst), dst_ld, int(rows), int(cols));
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
 cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count) {
   const long long total = static_cast<long long>(M) * N;
   long long blocks = (total + 255) / 256;
@@ -663,6 +729,16 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, co
 int gemm_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
               uint16_t* C, int64_t ldc, int layout, void* stream) {
   return dgt::run_gemm(dgt::KIND_BF16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream);
+}
+
+int gemm_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+              uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream) {
+  return dgt::run_gemm(dgt::KIND_E4M3, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue);
+}
+
+int gemm_e5m2(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+              uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream) {
+  return dgt::run_gemm(dgt::KIND_E5M2, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue);
 }
 
 int gemm_tf32_ex(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B, int64_t ldb, float* C,

@@ -44,25 +44,62 @@
 
 namespace dgt {
 
-enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_TF32 = 2 };
+// Operand kinds. The FP8 kinds (OCP E4M3 and E5M2 bytes) accumulate in fp32
+// like the others and write a bfloat16 C.
+enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_TF32 = 2, KIND_E4M3 = 3, KIND_E5M2 = 4 };
 
 template <int KIND>
 struct KindTraits;
 template <>
 struct KindTraits<KIND_F16> {
   using T = __half;
-  static constexpr uint32_t fmt = 0;  // instruction-descriptor operand format F16
+  static constexpr uint32_t fmt = 0;  // instruction-descriptor operand format F16 (kind::f16)
+  static constexpr int out = KIND_F16;
 };
 template <>
 struct KindTraits<KIND_BF16> {
   using T = __nv_bfloat16;
-  static constexpr uint32_t fmt = 1;  // BF16
+  static constexpr uint32_t fmt = 1;  // BF16 (kind::f16)
+  static constexpr int out = KIND_BF16;
 };
 template <>
 struct KindTraits<KIND_TF32> {
   using T = float;
-  static constexpr uint32_t fmt = 2;  // TF32
+  static constexpr uint32_t fmt = 2;  // TF32 (kind::tf32)
+  static constexpr int out = KIND_TF32;
 };
+template <>
+struct KindTraits<KIND_E4M3> {
+  using T = uint8_t;
+  static constexpr uint32_t fmt = 0;  // E4M3 (kind::f8f6f4)
+  static constexpr int out = KIND_BF16;
+};
+template <>
+struct KindTraits<KIND_E5M2> {
+  using T = uint8_t;
+  static constexpr uint32_t fmt = 1;  // E5M2 (kind::f8f6f4)
+  static constexpr int out = KIND_BF16;
+};
+
+// One tcgen05.mma of the kind's instruction family (single CTA / CTA pair).
+template <int KIND>
+__device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (KIND == KIND_TF32)
+    mma_tf32(d, a, b, idesc, acc);
+  else if constexpr (KIND == KIND_E4M3 || KIND == KIND_E5M2)
+    mma_f8f6f4(d, a, b, idesc, acc);
+  else
+    mma_f16(d, a, b, idesc, acc);
+}
+template <int KIND>
+__device__ __forceinline__ void mma_issue_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (KIND == KIND_TF32)
+    mma_tf32_pair(d, a, b, idesc, acc);
+  else if constexpr (KIND == KIND_E4M3 || KIND == KIND_E5M2)
+    mma_f8f6f4_pair(d, a, b, idesc, acc);
+  else
+    mma_f16_pair(d, a, b, idesc, acc);
+}
 
 // Status word codes (device status[0]); status[1] holds the epoch of the last aborted launch.
 enum : uint32_t {
@@ -661,10 +698,7 @@ __global__ void __launch_bounds__(320, 1)
             else
               bd = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
             const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            if constexpr (KIND == KIND_TF32)
-              mma_tf32(d, ad, bd, Cf::IDESC, acc);
-            else
-              mma_f16(d, ad, bd, Cf::IDESC, acc);
+            mma_issue<KIND>(d, ad, bd, Cf::IDESC, acc);
           }
           mma_commit(empty0 + 8 * s);  // frees the stage once these MMAs have read it
         }
@@ -691,7 +725,7 @@ __global__ void __launch_bounds__(320, 1)
       const int ncols = min(Cf::BN, p.N - nb * Cf::BN);
       const uint32_t stage = sE + warp * EPI_WARP_BYTES;
       for_each_acc_chunk(taddr, (ncols + 31) / 32, [&](int c, const uint32_t(&r)[32]) {
-        emit_chunk<KIND>(p, &tmC, stage, lane, row0, nb * Cf::BN + c * 32, r);
+        emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, nb * Cf::BN + c * 32, r);
       });
       tc_fence_before();
       __syncwarp();

@@ -268,10 +268,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
               const uint32_t acc = kk > 0 ? 1u : first;
-              if constexpr (KIND == KIND_TF32)
-                mma_tf32_pair(d, ad[kk], bd[kk], Cf::IDESC, acc);
-              else
-                mma_f16_pair(d, ad[kk], bd[kk], Cf::IDESC, acc);
+              mma_issue_pair<KIND>(d, ad[kk], bd[kk], Cf::IDESC, acc);
             }
             // every CTA whose loads land in stage s may refill it once all pairs are done with it
             mma_commit_pair(empty0 + 8 * s, uint16_t((1u << CL) - 1u));
@@ -311,7 +308,7 @@ __global__ void __launch_bounds__(192, 1)
       const int col0 = nbt * BN;
       if (wk.f < 0) {
         for_each_acc_chunk(taddr, nchunks,
-                           [&](int c, const uint32_t(&r)[32]) { emit_chunk<KIND>(p, &tmC, stage, lane, row0, col0 + c * 32, r); });
+                           [&](int c, const uint32_t(&r)[32]) { emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, r); });
       } else {
         // split tile: publish this segment's partial, then find out whether it is the last
         float4* mine = reinterpret_cast<float4*>(
@@ -355,7 +352,7 @@ __global__ void __launch_bounds__(192, 1)
               sum[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + cur[q].z);
               sum[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + cur[q].w);
             }
-            emit_chunk<KIND>(p, &tmC, stage, lane, row0, col0 + c * 32, sum);
+            emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, sum);
           });
         } else if (last) {
           // three or four segments: add them in segment order; this CTA's own one comes from tensor memory
@@ -384,7 +381,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t out[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) out[j] = __float_as_uint(acc[j]);
-            emit_chunk<KIND>(p, &tmC, stage, lane, row0, col0 + c * 32, out);
+            emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, out);
           });
         }
       }

@@ -23,13 +23,26 @@ struct LaunchPlan {
   cudaStream_t stream;
 };
 
-cudaError_t launch_f16(const LaunchPlan& L);
-cudaError_t launch_bf16(const LaunchPlan& L);
-cudaError_t launch_tf32(const LaunchPlan& L);
-int pair_clusters_f16(bool kmajor, int bn, int pairs);
-int pair_clusters_bf16(bool kmajor, int bn, int pairs);
-int pair_clusters_tf32(bool kmajor, int bn, int pairs);
+// Kernel launch and co-resident cluster count for one (kind, B layout); each
+// pair is defined in its own translation unit (gemm_<kind>_<layout>.cu, built
+// in parallel). The FP8 kinds exist for K-major B only (a row-major B is
+// transposed into scratch first).
+#define DGT_DECLARE_VARIANTS(name)                 \
+  cudaError_t launch_##name(const LaunchPlan& L);  \
+  int pair_clusters_##name(int bn, int pairs);
+DGT_DECLARE_VARIANTS(f16_rm)
+DGT_DECLARE_VARIANTS(f16_km)
+DGT_DECLARE_VARIANTS(bf16_rm)
+DGT_DECLARE_VARIANTS(bf16_km)
+DGT_DECLARE_VARIANTS(tf32_rm)
+DGT_DECLARE_VARIANTS(tf32_km)
+DGT_DECLARE_VARIANTS(e4m3_km)
+DGT_DECLARE_VARIANTS(e5m2_km)
+#undef DGT_DECLARE_VARIANTS
 cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count);
+// dst[n][k] = src[k][n] for a rows x cols byte matrix (leading dimensions in bytes).
+cudaError_t launch_transpose_bytes(const void* src, int64_t src_ld, void* dst, int64_t dst_ld, int64_t rows,
+                                   int64_t cols, cudaStream_t stream, int sm_count);
 // The K = 0 product with a fused epilogue (epilogue_only_kernel).
 cudaError_t launch_epilogue_only(int kind, void* C, long long ldc, int M, int N, const GemmParams& p,
                                  cudaStream_t stream, int sm_count);
@@ -176,17 +189,17 @@ int pair_clusters_width(int bn) {
   }
 }
 
-template <int KIND>
-int pair_clusters_kind(bool kmajor, int bn, int pairs) {
-  if (pairs == 1) return kmajor ? pair_clusters_width<KIND, true, 1>(bn) : pair_clusters_width<KIND, false, 1>(bn);
-  if (pairs == 2) return kmajor ? pair_clusters_width<KIND, true, 2>(bn) : pair_clusters_width<KIND, false, 2>(bn);
-  return 0;
-}
-
-template <int KIND>
-cudaError_t launch_kind(const LaunchPlan& L) {
-  if (L.pair) return L.b_kmajor ? launch_pair_layout<KIND, true>(L) : launch_pair_layout<KIND, false>(L);
-  return L.b_kmajor ? launch_layout<KIND, true>(L) : launch_layout<KIND, false>(L);
-}
+// Body of one gemm_<kind>_<layout>.cu: instantiates every kernel of that kind
+// and B layout (single CTA, CTA pair, two pairs; each tile width).
+#define DGT_DEFINE_VARIANTS(name, KIND, KMAJ)                                          \
+  cudaError_t launch_##name(const LaunchPlan& L) {                                     \
+    if (L.b_kmajor != (KMAJ)) return cudaErrorInvalidValue;                            \
+    return L.pair ? launch_pair_layout<KIND, KMAJ>(L) : launch_layout<KIND, KMAJ>(L);  \
+  }                                                                                    \
+  int pair_clusters_##name(int bn, int pairs) {                                        \
+    if (pairs == 1) return pair_clusters_width<KIND, KMAJ, 1>(bn);                     \
+    if (pairs == 2) return pair_clusters_width<KIND, KMAJ, 2>(bn);                     \
+    return 0;                                                                          \
+  }
 
 }  // namespace dgt

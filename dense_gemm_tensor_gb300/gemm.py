@@ -45,7 +45,7 @@ class Epilogue(ctypes.Structure):
                 ("activation", ctypes.c_int)]
 
 # Every symbol the C header declares.
-EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_tf32_ex", "gemm_f16_ex", "gemm_bf16_ex",
+EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_tf32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_e4m3", "gemm_e5m2",
            "gemm_status_string", "gemm_get_device_status", "gemm_reset_device_status", "gemm_set_debug",
            "gemm_launch_count", "gemm_set_tuning", "gemm_last_plan", "gemm_free_workspaces",
            "gemm_bf16_static_scratch")
@@ -73,7 +73,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, vp]
         fn.restype = ctypes.c_int
-    for name in ("gemm_tf32_ex", "gemm_f16_ex", "gemm_bf16_ex"):
+    for name in ("gemm_tf32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_e4m3", "gemm_e5m2"):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, ctypes.POINTER(Epilogue), vp]
         fn.restype = ctypes.c_int
@@ -128,13 +128,15 @@ def gemm_bf16_static_scratch(M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_
 
 def gemm_ex(dtype_name, M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_MAJOR, epilogue=None,
             stream=None) -> int:
-    """gemm_{tf32,f16,bf16}_ex with raw device pointers; `epilogue` an Epilogue or None."""
-    fn = getattr(load(), f"gemm_{dtype_name}_ex")
+    """gemm_{tf32,f16,bf16}_ex or gemm_{e4m3,e5m2} with raw device pointers;
+    `epilogue` an Epilogue or None."""
+    fn = getattr(load(), f"gemm_{dtype_name}" + ("" if dtype_name in ("e4m3", "e5m2") else "_ex"))
     return fn(M, N, K, A, lda, B, ldb, C, ldc, layout, ctypes.byref(epilogue) if epilogue is not None else None,
               stream)
 
 
 _BY_DTYPE = {torch.float32: "gemm_tf32", torch.float16: "gemm_f16", torch.bfloat16: "gemm_bf16"}
+_FP8 = {torch.float8_e4m3fn: "gemm_e4m3", torch.float8_e5m2: "gemm_e5m2"}
 _FN = {}  # dtype -> bound C function, filled on first use
 _FN_EX = {}
 
@@ -161,11 +163,15 @@ def matmul(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *,
     transposed) for ``layout=GEMM_B_K_MAJOR``. Rows may be padded (stride(0) >
     row length) but elements along a row must be contiguous. The dtype selects
     the entry point: float32 -> gemm_tf32, float16 -> gemm_f16, bfloat16 ->
-    gemm_bf16 (the *_ex variants with an epilogue). ``out`` (M x N, same dtype)
-    may have padded rows too; with beta != 0 it supplies the C that is scaled
-    and added. ``bias``: N elements of the same dtype, contiguous.
+    gemm_bf16 (the *_ex variants with an epilogue); float8_e4m3fn ->
+    gemm_e4m3 and float8_e5m2 -> gemm_e5m2, whose C is bfloat16. ``out`` (M x
+    N, the output dtype) may have padded rows too; with beta != 0 it supplies
+    the C that is scaled and added. ``bias``: N elements of the output dtype,
+    contiguous.
     """
     dt = A.dtype
+    if dt in _FP8:
+        return _matmul_fp8(A, B, out, layout, stream, alpha, beta, bias, activation)
     fn = _FN.get(dt)
     if fn is None:
         if dt not in _BY_DTYPE:
@@ -210,6 +216,40 @@ def matmul(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *,
               out.data_ptr() or None, _rows(out, "out"), layout, ctypes.byref(epi), s)
     if code != GEMM_OK:
         raise GemmError(code, _BY_DTYPE[dt] + "_ex")
+    return out
+
+
+def _matmul_fp8(A, B, out, layout, stream, alpha, beta, bias, activation):
+    dt = A.dtype
+    if B.dtype != dt:
+        raise TypeError("A and B must have the same FP8 dtype")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    M, K = A.shape
+    if layout == GEMM_B_ROW_MAJOR:
+        if B.shape[0] != K:
+            raise ValueError("B must be K x N")
+        N = B.shape[1]
+    else:
+        if B.shape[1] != K:
+            raise ValueError("B must be N x K for the K-major layout")
+        N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (M, N):
+        raise ValueError("out must be M x N bfloat16")
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(k for k in ACTIVATIONS if k)}")
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.dim() != 1 or bias.numel() != N or
+                             not bias.is_cuda or (N > 1 and bias.stride(0) != 1)):
+        raise ValueError("bias must be a contiguous CUDA bfloat16 vector of N elements")
+    epi = Epilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None, ACTIVATIONS[activation])
+    s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    fn = getattr(load(), _FP8[dt])
+    code = fn(M, N, K, A.data_ptr() or None, _rows(A, "A"), B.data_ptr() or None, _rows(B, "B"),
+              out.data_ptr() or None, _rows(out, "out"), layout, ctypes.byref(epi), s)
+    if code != GEMM_OK:
+        raise GemmError(code, _FP8[dt])
     return out
 
 

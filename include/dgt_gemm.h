@@ -144,6 +144,25 @@ int gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda
                  uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream);
 
 /*
+ * FP8 products: A and B hold OCP FP8 bytes -- E4M3 (gemm_e4m3: 1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits; no infinities, S.1111.111 is
+ * NaN; largest finite 448) or E5M2 (gemm_e5m2: 1 sign, 5 exponent bits with
+ * bias 15, 2 mantissa bits, IEEE-style infinities and NaNs; largest finite
+ * 57344) -- both operands in the same format. Products are exact and
+ * accumulate in fp32 (tcgen05.mma kind::f8f6f4); C is bfloat16 (uint16_t bit
+ * patterns, RNE), after the optional fused epilogue (alpha carries per-tensor
+ * scales). The GEMM pages name FP8 as a possible follow-up only; these calls
+ * go beyond them. Layouts, leading dimensions (in elements = bytes for A and
+ * B), ownership, asynchrony and errors are those of the calls above. A
+ * row-major B (layout 0) is first transposed into the stream's scratch (one
+ * extra pass over B); a K-major B (layout 1) is read in place.
+ */
+int gemm_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+              uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream);
+int gemm_e5m2(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+              uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream);
+
+/*
  * gemm_bf16_static_scratch: gemm_bf16 for callers that cannot allocate.
  * (The GEMM pages have no counterpart to this call.)
  *
