@@ -66,25 +66,45 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint8_t* __restric
 
 // dst[n][k] = src[k][n] for a rows x cols byte matrix (rows = K, cols = N):
 // a row-major K x N FP8 B becomes the K-major N x K operand the FP8 kernels
-// read. 32 x 32 tiles through shared memory (reads along src rows, writes
-// along dst rows); the tiles are strided over the grid.
+// read. 64 x 64-byte tiles through shared memory: 256 threads read the tile's
+// rows as 4-byte words (bytes at a ragged or unaligned edge), and write the
+// transposed rows as 4-byte words gathered from four tile rows. The tiles are
+// strided over the grid. dst_ld is a multiple of 64 no smaller than rows
+// rounded up to 64, so the words past `rows` land in the row's padding.
 __global__ void __launch_bounds__(256) transpose_bytes_kernel(const uint8_t* __restrict__ src, long long src_ld,
                                                               uint8_t* __restrict__ dst, long long dst_ld,
-                                                              int rows, int cols) {
-  __shared__ uint8_t tile[32][33];
-  const int tiles_c = (cols + 31) / 32;
-  const long long ntiles = static_cast<long long>((rows + 31) / 32) * tiles_c;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
-  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const int r0 = static_cast<int>(t / tiles_c) * 32, c0 = static_cast<int>(t % tiles_c) * 32;
-    for (int i = ty; i < 32; i += 8) {
-      const int r = r0 + i, c = c0 + tx;
-      tile[i][tx] = (r < rows && c < cols) ? src[static_cast<long long>(r) * src_ld + c] : uint8_t(0);
+                                                              int rows, int cols, int src_words) {
+  __shared__ __align__(16) uint8_t tile[64][68];
+  const int tiles_c = (cols + 63) / 64;
+  const long long ntiles = static_cast<long long>((rows + 63) / 64) * tiles_c;
+  const int t = threadIdx.x;
+  for (long long tt = blockIdx.x; tt < ntiles; tt += gridDim.x) {
+    const int r0 = static_cast<int>(tt / tiles_c) * 64, c0 = static_cast<int>(tt % tiles_c) * 64;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = (t >> 4) + 16 * i, w = t & 15;  // tile row, word
+      const int gr = r0 + r, gc = c0 + 4 * w;
+      uint32_t v = 0;
+      if (gr < rows) {
+        const uint8_t* p = src + static_cast<long long>(gr) * src_ld + gc;
+        if (src_words && gc + 3 < cols) {
+          v = *reinterpret_cast<const uint32_t*>(p);
+        } else {
+          for (int j = 0; j < 4; ++j)
+            if (gc + j < cols) v |= uint32_t(p[j]) << (8 * j);
+        }
+      }
+      *reinterpret_cast<uint32_t*>(&tile[r][4 * w]) = v;
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-      const int c = c0 + i, r = r0 + tx;  // dst row c, column r
-      if (c < cols && r < rows) dst[static_cast<long long>(c) * dst_ld + r] = tile[tx][i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = (t >> 4) + 16 * i, w = t & 15;  // dst row (tile column), word
+      if (c0 + c < cols) {
+        const uint32_t v = uint32_t(tile[4 * w][c]) | (uint32_t(tile[4 * w + 1][c]) << 8) |
+                           (uint32_t(tile[4 * w + 2][c]) << 16) | (uint32_t(tile[4 * w + 3][c]) << 24);
+        *reinterpret_cast<uint32_t*>(dst + static_cast<long long>(c0 + c) * dst_ld + r0 + 4 * w) = v;
+      }
     }
     __syncthreads();
   }
@@ -692,10 +712,13 @@ cudaError_t launch_epilogue_only(int kind, void* C, long long ldc, int M, int N,
 
 cudaError_t launch_transpose_bytes(const void* src, int64_t src_ld, void* dst, int64_t dst_ld, int64_t rows,
                                    int64_t cols, cudaStream_t stream, int sm_count) {
-  const long long tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
-  long long blocks = tiles < 16LL * sm_count ? tiles : 16LL * sm_count;
+  const long long tiles = ((rows + 63) / 64) * ((cols + 63) / 64);
+  long long blocks = tiles < 8LL * sm_count ? tiles : 8LL * sm_count;
+  // 4-byte source words where every row start is 4-byte aligned
+  const int words = ((reinterpret_cast<uintptr_t>(src) | static_cast<uintptr_t>(src_ld)) % 4) == 0;
   transpose_bytes_kernel<<<int(blocks), 256, 0, stream>>>(static_cast<const uint8_t*>(src), src_ld,
-                                                          static_cast<uint8_t*>(dst), dst_ld, int(rows), int(cols));
+                                                          static_cast<uint8_t*>(dst), dst_ld, int(rows), int(cols),
+                                                          words);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
   return e;
