@@ -212,16 +212,21 @@ int granularity(const void* p, int64_t ld, int es) {
   return g;
 }
 
-bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+// 3-D tiled tensor map: x innermost (contiguous), y rows `row_bytes` apart, z
+// matrices of a batch `mat_bytes` apart (depth 1 for one product, whose z is
+// always 0). Boxes are box_inner x box_outer x 1.
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint64_t depth, uint64_t mat_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encoder();
   if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+  if (depth == 1) mat_bytes = row_bytes * outer;  // never stepped; a stride that spans the matrix
+  if (mat_bytes == 0 || mat_bytes % 16 != 0 || mat_bytes >= (uint64_t(1) << 40)) return false;
+  cuuint64_t dims[3] = {inner, outer, depth};
+  cuuint64_t strides[2] = {row_bytes, mat_bytes};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -344,7 +349,7 @@ constexpr double kSlabCycles[3][4] = {
 // least total time wins. The band height keeps a band's A rows and the B tiles
 // in flight inside L2.
 TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es, bool kmajor, bool all_tma,
-                     int sms) {
+                     int sms, int64_t nbat = 1) {
   const int64_t kslabs = (K * es + 127) / 128;
   const int fv = g_force_variant.load(std::memory_order_relaxed);
   const int fb = g_force_bn.load(std::memory_order_relaxed);
@@ -368,7 +373,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
     const double slab = kSlabCycles[pair ? pairs : 0][wi];
     const int64_t rows = pair ? 256 : 128;
     const int64_t tiles_n = (N + bn - 1) / bn;
-    const int64_t tiles = ((M + rows - 1) / rows) * ((tiles_n + pairs - 1) / pairs);
+    const int64_t tiles = nbat * ((M + rows - 1) / rows) * ((tiles_n + pairs - 1) / pairs);
     const int64_t full = tiles / conc, rest = tiles % conc;
     // pair kernel: the tiles of the last partial round may be split along K
     // into `segs` pieces run by different pairs (fp32 partials summed at the end)
@@ -413,16 +418,21 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
   for (int bn : kPairTileWidths) consider(true, 1, bn);
   for (int bn : kTileWidths) consider(false, 1, bn);
   if (best_cost < 0) {  // a forced combination that does not apply: fall back to the single-CTA default
-    const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
+    const int64_t tiles = nbat * ((M + 127) / 128) * ((N + 255) / 256);
     best = TilePlan{false, 1, 256, 8, int(tiles < sms ? tiles : sms), 1, sms};
   }
   if (fr) best.raster = fr;
   return best;
 }
 
+// Strided batch of products (batch = 1: one product; strides in elements).
+struct Batch {
+  int64_t count = 1, stride_a = 0, stride_b = 0, stride_c = 0;
+};
+
 int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
              void* C, int64_t ldc, int layout, void* stream_ptr, const ExternalScratch* ext = nullptr,
-             const gemm_epilogue_t* epi = nullptr) {
+             const gemm_epilogue_t* epi = nullptr, const Batch& bat = Batch()) {
   const bool fp8 = kind == KIND_E4M3 || kind == KIND_E5M2;
   const int es = (kind == KIND_TF32) ? 4 : fp8 ? 1 : 2;  // operand element size
   const int eo = (kind == KIND_TF32) ? 4 : 2;             // output element size (FP8 writes bfloat16)
@@ -430,15 +440,27 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   const int64_t kLim = (int64_t(1) << 31) - 1;
   if (M < 0 || N < 0 || K < 0 || M > kLim || N > kLim || K > kLim) return GEMM_ERR_INVALID_VALUE;
   if (layout != GEMM_B_ROW_MAJOR && layout != GEMM_B_K_MAJOR) return GEMM_ERR_INVALID_VALUE;
-  if (M == 0 || N == 0) return GEMM_OK;
+  const int64_t nbat = bat.count;
+  if (nbat < 0 || bat.stride_a < 0 || bat.stride_b < 0 || bat.stride_c < 0) return GEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0 || nbat == 0) return GEMM_OK;
   if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_VALUE;
+  if (nbat > 1) {
+    // the C matrices must not overlap one another; A and B may repeat (stride 0) but not overlap partly
+    if (bat.stride_c < (M - 1) * ldc + N) return GEMM_ERR_INVALID_VALUE;
+    if (K > 0 && bat.stride_a != 0 && bat.stride_a < (M - 1) * lda + K) return GEMM_ERR_INVALID_VALUE;
+    const int64_t b_ext = layout == GEMM_B_ROW_MAJOR ? (K - 1) * ldb + N : (N - 1) * ldb + K;
+    if (K > 0 && bat.stride_b != 0 && bat.stride_b < b_ext) return GEMM_ERR_INVALID_VALUE;
+    if (bat.stride_a > (int64_t(1) << 40) || bat.stride_b > (int64_t(1) << 40) || bat.stride_c > (int64_t(1) << 40))
+      return GEMM_ERR_INVALID_VALUE;
+    if (nbat > kLim) return GEMM_ERR_INVALID_VALUE;
+  }
   if (K > 0) {
     if (A == nullptr || B == nullptr || lda < K) return GEMM_ERR_INVALID_VALUE;
     if (ldb < (layout == GEMM_B_ROW_MAJOR ? N : K)) return GEMM_ERR_INVALID_VALUE;
     if (lda > (int64_t(1) << 40) / es || ldb > (int64_t(1) << 40) / es) return GEMM_ERR_INVALID_VALUE;
   }
   if (ldc > (int64_t(1) << 40) / eo) return GEMM_ERR_INVALID_VALUE;
-  if (((M + 127) / 128) * ((N + 127) / 128) > kLim) return GEMM_ERR_INVALID_VALUE;
+  if (((M + 127) / 128) * ((N + 127) / 128) > kLim / nbat) return GEMM_ERR_INVALID_VALUE;
 
   if (epi != nullptr && (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU_TANH))
     return GEMM_ERR_INVALID_VALUE;
@@ -456,6 +478,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
 
   uintptr_t c0, c1;
   extent(C, M, N, ldc, eo, &c0, &c1);
+  c1 += static_cast<uintptr_t>((nbat - 1) * bat.stride_c * eo);  // every matrix of the batch
   if (!is_device_memory(C)) return GEMM_ERR_NOT_DEVICE_MEMORY;
   if (bias != nullptr) {
     const uintptr_t s0 = reinterpret_cast<uintptr_t>(bias), s1 = s0 + uintptr_t(N) * eo;
@@ -465,20 +488,23 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   if (K == 0) {
-    cudaError_t e;
-    if (fused) {
-      GemmParams ep;
-      memset(&ep, 0, sizeof(ep));
-      ep.alpha = epi->alpha;
-      ep.beta = epi->beta;
-      ep.bias = bias;
-      ep.act = epi->activation;
-      e = launch_epilogue_only(out_kind, C, ldc, int(M), int(N), ep, stream, dev->sm_count);
-    } else {
-      e = launch_fill_zero(C, ldc, int(M), int(N), eo, stream, dev->sm_count);
+    for (int64_t z = 0; z < nbat; ++z) {
+      void* Cz = static_cast<char*>(C) + z * bat.stride_c * eo;
+      cudaError_t e;
+      if (fused) {
+        GemmParams ep;
+        memset(&ep, 0, sizeof(ep));
+        ep.alpha = epi->alpha;
+        ep.beta = epi->beta;
+        ep.bias = bias;
+        ep.act = epi->activation;
+        e = launch_epilogue_only(out_kind, Cz, ldc, int(M), int(N), ep, stream, dev->sm_count);
+      } else {
+        e = launch_fill_zero(Cz, ldc, int(M), int(N), eo, stream, dev->sm_count);
+      }
+      if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
+      g_launches.fetch_add(1, std::memory_order_relaxed);
     }
-    if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
     return GEMM_OK;
   }
 
@@ -488,6 +514,8 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     extent(B, K, N, ldb, es, &b0, &b1);
   else
     extent(B, N, K, ldb, es, &b0, &b1);
+  a1 += static_cast<uintptr_t>((nbat - 1) * bat.stride_a * es);
+  b1 += static_cast<uintptr_t>((nbat - 1) * bat.stride_b * es);
   if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return GEMM_ERR_INVALID_VALUE;
   if (!is_device_memory(A) || !is_device_memory(B)) return GEMM_ERR_NOT_DEVICE_MEMORY;
 
@@ -495,6 +523,11 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   memset(&L, 0, sizeof(L));
   GemmParams& p = L.p;
   int ga = granularity(A, lda, es), gb = granularity(B, ldb, es);
+  if (nbat > 1) {
+    // a batch is streamed by TMA in place: rows and matrix strides on 16-byte boundaries
+    if (ga < 16 || gb < 16 || (bat.stride_a * es) % 16 != 0 || (bat.stride_b * es) % 16 != 0 || fp8)
+      return GEMM_ERR_MISALIGNED;
+  }
   // The FP8 kernels read B K-major only: a row-major FP8 B is transposed into
   // the stream's scratch first (the packed-B slot), and from then on it is K-major.
   const bool transpose_b = fp8 && layout == GEMM_B_ROW_MAJOR;
@@ -511,8 +544,8 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   // copy pays for itself once the other output dimension is a few thousand.
   // FP8 operands always go through TMA (the copy warps do not handle 1-byte
   // granules), so they are packed whenever they need it.
-  const bool may_pack =
-      ext == nullptr && (fp8 || !(g_debug_flags.load(std::memory_order_relaxed) & DEBUG_NO_PACK));
+  const bool may_pack = nbat == 1 && ext == nullptr &&
+                        (fp8 || !(g_debug_flags.load(std::memory_order_relaxed) & DEBUG_NO_PACK));
   auto off_line = [es](const void* ptr, int64_t ld) {
     return ((reinterpret_cast<uintptr_t>(ptr) | static_cast<uintptr_t>(ld * es)) % 128) != 0;
   };
@@ -520,7 +553,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   const bool pack_a = may_pack && (ga < 16 || (big && N >= 2048 && off_line(A, lda)));
   const bool pack_b = may_pack && (transpose_b || gb < 16 || (big && M >= 2048 && off_line(B, ldb)));
   TilePlan plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, (ga == 16 || pack_a) && (gb == 16 || pack_b),
-                              dev->sm_count);
+                              dev->sm_count, nbat);
   // Scratch for this plan, laid out as [counters][split partials][packed A][packed B].
   const int64_t lda_p = pack_a ? (K * es + 127) / 128 * 128 / es : lda;
   const int64_t b_rows = kmajor ? N : K, b_cols = kmajor ? K : N;  // of the operand the kernel reads
@@ -528,7 +561,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   auto split_tiles = [&](const TilePlan& pl) {
     const int64_t tm = (M + (pl.pair ? 255 : 127)) / (pl.pair ? 256 : 128);
     const int64_t tn = ((N + pl.bn - 1) / pl.bn + pl.pairs - 1) / pl.pairs;
-    const int64_t r = (pl.pair && pl.segs > 1) ? (tm * tn) % pl.conc : 0;
+    const int64_t r = (pl.pair && pl.segs > 1) ? (nbat * tm * tn) % pl.conc : 0;
     return (r > 0 && r <= 1024) ? int(r) : 0;
   };
   int rest = split_tiles(plan);
@@ -547,7 +580,8 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     if (ws == nullptr) {
       // no scratch: no split tail, and unaligned operands are read in place by the copy warps
       if (fp8 && (pack_a || pack_b)) return GEMM_ERR_LAUNCH;  // FP8 cannot do without the packed copy
-      if (pack_a || pack_b) plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, ga == 16 && gb == 16, dev->sm_count);
+      if (pack_a || pack_b)
+        plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, ga == 16 && gb == 16, dev->sm_count, nbat);
       rest = 0;
     }
   }
@@ -561,7 +595,12 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   p.K = int(K);
   p.tiles_m = int(tiles_m);
   p.tiles_n = int(tiles_n);
-  p.num_tiles = int(tiles_m * tiles_n);
+  p.batch = int(nbat);
+  p.tiles_per_batch = int(tiles_m * tiles_n);
+  p.num_tiles = int(nbat * tiles_m * tiles_n);
+  p.stride_a = nbat > 1 ? bat.stride_a : 0;
+  p.stride_b = nbat > 1 ? bat.stride_b : 0;
+  p.stride_c = nbat > 1 ? bat.stride_c : 0;
   p.num_kb = int((K * es + 127) / 128);
   p.raster = plan.raster;
   p.tail_start = p.num_tiles;
@@ -628,22 +667,25 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   const CUtensorMapDataType dt_out = fp8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : dt;
   const uint32_t bk = 128 / es;  // K elements per 128-byte row
   // A box: 128 rows, or 64 where two pairs each load half a CTA's rows for both
-  if (p.a_tma && !encode_2d(&L.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda) * es, bk,
-                            (plan.pair && plan.pairs == 2) ? 64 : 128))
+  const uint64_t za = p.stride_a ? uint64_t(nbat) : 1, zb = p.stride_b ? uint64_t(nbat) : 1;
+  if (p.a_tma && !encode_3d(&L.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda) * es, za,
+                            uint64_t(p.stride_a) * es, bk, (plan.pair && plan.pairs == 2) ? 64 : 128))
     return GEMM_ERR_DRIVER;
   if (p.b_tma) {
     bool ok;
     if (kmajor) {
-      ok = encode_2d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, bk,
+      ok = encode_3d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, zb, uint64_t(p.stride_b) * es, bk,
                      uint32_t(plan.pair ? bn / 2 : bn));
     } else {
-      ok = encode_2d(&L.tmB, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, 128 / es, bk,
-                     es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode_3d(&L.tmB, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, zb, uint64_t(p.stride_b) * es,
+                     128 / es, bk, es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
     }
     if (!ok) return GEMM_ERR_DRIVER;
   }
   // C box: 32 rows x 64 bytes, the staging tile of one epilogue warp (64-byte swizzle)
-  if (p.c_tma && !encode_2d(&L.tmC, dt_out, C, uint64_t(N), uint64_t(M), uint64_t(ldc) * eo, uint32_t(64 / eo), 32,
+  if (p.c_tma && (p.stride_c * eo) % 16 != 0) p.c_tma = 0;  // matrices of C off 16-byte boundaries: row stores
+  if (p.c_tma && !encode_3d(&L.tmC, dt_out, C, uint64_t(N), uint64_t(M), uint64_t(ldc) * eo,
+                            p.stride_c ? uint64_t(nbat) : 1, uint64_t(p.stride_c) * eo, uint32_t(64 / eo), 32,
                             CU_TENSOR_MAP_SWIZZLE_64B))
     return GEMM_ERR_DRIVER;
   L.b_kmajor = kmajor;
@@ -752,6 +794,29 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, co
 int gemm_bf16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
               uint16_t* C, int64_t ldc, int layout, void* stream) {
   return dgt::run_gemm(dgt::KIND_BF16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream);
+}
+
+int gemm_tf32_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                              int64_t stride_a, const float* B, int64_t ldb, int64_t stride_b, float* C, int64_t ldc,
+                              int64_t stride_c, int layout, const gemm_epilogue_t* epilogue, void* stream) {
+  const dgt::Batch b{batch, stride_a, stride_b, stride_c};
+  return dgt::run_gemm(dgt::KIND_TF32, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue, b);
+}
+
+int gemm_f16_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                             int64_t stride_a, const uint16_t* B, int64_t ldb, int64_t stride_b, uint16_t* C,
+                             int64_t ldc, int64_t stride_c, int layout, const gemm_epilogue_t* epilogue,
+                             void* stream) {
+  const dgt::Batch b{batch, stride_a, stride_b, stride_c};
+  return dgt::run_gemm(dgt::KIND_F16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue, b);
+}
+
+int gemm_bf16_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                              int64_t stride_a, const uint16_t* B, int64_t ldb, int64_t stride_b, uint16_t* C,
+                              int64_t ldc, int64_t stride_c, int layout, const gemm_epilogue_t* epilogue,
+                              void* stream) {
+  const dgt::Batch b{batch, stride_a, stride_b, stride_c};
+  return dgt::run_gemm(dgt::KIND_BF16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue, b);
 }
 
 int gemm_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,

@@ -117,6 +117,11 @@ enum : uint32_t {
 
 struct GemmParams {
   int M, N, K;
+  // Strided batch: matrix z of A, B, C starts stride_{a,b,c} elements after
+  // matrix z-1 (a stride of 0 repeats one matrix); batch = 1 for one product.
+  // Work tiles run batch by batch: tile t belongs to matrix t / tiles_per_batch.
+  int batch, tiles_per_batch;
+  long long stride_a, stride_b, stride_c;
   int tiles_m, tiles_n, num_tiles, num_kb;
   int raster;  // band height (in tiles along M) of the tile order
   // Work items: tiles [0, tail_start) in tile order, whole; each tile from
@@ -195,10 +200,13 @@ struct Cfg {
                                     (uint32_t(BM >> 4) << 24);
 };
 
-// Linear work id -> output tile. Tiles go in bands of `raster` tile-rows: down
-// the band's rows first, then across N, band after band. A band's B tiles and
-// its A row-tiles stay in L2 while the band is worked on.
-__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
+// Linear work id -> output tile (mb, nb) of matrix bz of the batch. Within a
+// matrix, tiles go in bands of `raster` tile-rows: down the band's rows
+// first, then across N, band after band. A band's B tiles and its A
+// row-tiles stay in L2 while the band is worked on.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb, int& bz) {
+  bz = t / p.tiles_per_batch;
+  t -= bz * p.tiles_per_batch;
   const int band = p.raster * p.tiles_n;
   const int g = t / band;
   const int first_m = g * p.raster;
@@ -389,13 +397,13 @@ __device__ __forceinline__ void epi_get_row(uint32_t stage, int lane, uint32_t (
 // Writes the staged tile to C[row0 .., col0 ..] (see above).
 template <int KIND>
 __device__ __forceinline__ void epi_flush(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage, int lane,
-                                          int row0, int col0) {
+                                          int row0, int col0, int bz) {
   constexpr int ROUND_COLS = KIND == KIND_TF32 ? 16 : 32;
   if (p.c_tma && col0 + ROUND_COLS <= p.N) {
     fence_proxy_async_smem();  // make the tile visible to the TMA unit
     __syncwarp();
     if (lane == 0 && row0 < p.M && col0 < p.N) {
-      tma_store_2d(tmC, stage, col0, row0);
+      tma_store_3d(tmC, stage, col0, row0, bz);
       bulk_commit_group();
     }
   } else {
@@ -409,7 +417,7 @@ __device__ __forceinline__ void epi_flush(const GemmParams& p, const CUtensorMap
       const int row = row0 + r;
       const uint32_t v = ld_shared_u32(epi_chunk_addr(stage, r, l >> 2) + ((l & 3) << 2));
       if (row < p.M && col < p.N) {
-        uint8_t* dst = reinterpret_cast<uint8_t*>(p.C) + (static_cast<long long>(row) * p.ldc + col) * ES;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.C) + (bz * p.stride_c + static_cast<long long>(row) * p.ldc + col) * ES;
         if (ES == 4 || (p.c_gran >= 4 && col + 1 < p.N)) {
           *reinterpret_cast<uint32_t*>(dst) = v;
         } else {
@@ -425,7 +433,8 @@ __device__ __forceinline__ void epi_flush(const GemmParams& p, const CUtensorMap
 // Loads C's current 32 x 64-byte block at (row0, col0) into the tile with
 // coalesced loads (the mirror of the row-wise stores); zeros outside M x N.
 template <int KIND>
-__device__ __forceinline__ void epi_load_c(const GemmParams& p, uint32_t stage, int lane, int row0, int col0) {
+__device__ __forceinline__ void epi_load_c(const GemmParams& p, uint32_t stage, int lane, int row0, int col0,
+                                           int bz) {
   constexpr int ES = KIND == KIND_TF32 ? 4 : 2;
   const int l = lane & 15;
   const int col = col0 + l * (4 / ES);
@@ -436,7 +445,7 @@ __device__ __forceinline__ void epi_load_c(const GemmParams& p, uint32_t stage, 
     uint32_t v = 0;
     if (row < p.M && col < p.N) {
       const uint8_t* src =
-          reinterpret_cast<const uint8_t*>(p.C) + (static_cast<long long>(row) * p.ldc + col) * ES;
+          reinterpret_cast<const uint8_t*>(p.C) + (bz * p.stride_c + static_cast<long long>(row) * p.ldc + col) * ES;
       if (ES == 4 || (p.c_gran >= 4 && col + 1 < p.N)) {
         v = *reinterpret_cast<const uint32_t*>(src);
       } else {
@@ -480,7 +489,7 @@ __device__ __forceinline__ float epi_activation(float v, int act) {
 // are r[OFF .. OFF + 63 / ES] (32 for 16-bit C, 16 for fp32 C).
 template <int KIND, int OFF>
 __device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage,
-                                                int lane, int row0, int col0, const uint32_t (&r)[32]) {
+                                                int lane, int row0, int col0, int bz, const uint32_t (&r)[32]) {
   constexpr int RC = KIND == KIND_TF32 ? 16 : 32;
   using T = typename KindTraits<KIND>::T;
   epi_acquire(p, lane);
@@ -488,7 +497,7 @@ __device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUten
 #pragma unroll
   for (int k = 0; k < RC; ++k) v[k] = p.alpha * __uint_as_float(r[OFF + k]);
   if (p.beta != 0.0f) {
-    epi_load_c<KIND>(p, stage, lane, row0, col0);
+    epi_load_c<KIND>(p, stage, lane, row0, col0, bz);
     uint32_t w[16];
     epi_get_row(stage, lane, w);
 #pragma unroll
@@ -519,18 +528,19 @@ __device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUten
                          __float_as_uint(epi_activation(v[2 * k + 1], p.act)));
   }
   epi_put_row(stage, lane, w);
-  epi_flush<KIND>(p, tmC, stage, lane, row0, col0);
+  epi_flush<KIND>(p, tmC, stage, lane, row0, col0, bz);
 }
 
 // Converts 32 accumulator columns of the warp's 32 rows (lane = row, values
-// in r) to the output type and writes them to C[row0 .., col0 .. col0+31],
-// through the fused epilogue when the launch has one. Warp-collective.
+// in r) to the output type and writes them to C[row0 .., col0 .. col0+31] of
+// matrix bz, through the fused epilogue when the launch has one.
+// Warp-collective.
 template <int KIND>
 __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage, int lane,
-                                           int row0, int col0, const uint32_t (&r)[32]) {
+                                           int row0, int col0, int bz, const uint32_t (&r)[32]) {
   if (p.fused) {
-    epi_round_fused<KIND, 0>(p, tmC, stage, lane, row0, col0, r);
-    if (KIND == KIND_TF32 && col0 + 16 < p.N) epi_round_fused<KIND, 16>(p, tmC, stage, lane, row0, col0 + 16, r);
+    epi_round_fused<KIND, 0>(p, tmC, stage, lane, row0, col0, bz, r);
+    if (KIND == KIND_TF32 && col0 + 16 < p.N) epi_round_fused<KIND, 16>(p, tmC, stage, lane, row0, col0 + 16, bz, r);
     return;
   }
   if constexpr (KIND == KIND_TF32) {
@@ -542,7 +552,7 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
       for (int j = 0; j < 16; ++j) w[j] = r[16 * h + j];
       epi_acquire(p, lane);
       epi_put_row(stage, lane, w);
-      epi_flush<KIND>(p, tmC, stage, lane, row0, col0 + 16 * h);
+      epi_flush<KIND>(p, tmC, stage, lane, row0, col0 + 16 * h, bz);
     }
   } else {
     uint32_t w[16];
@@ -550,7 +560,7 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
     for (int j = 0; j < 16; ++j) w[j] = pack2<KIND>(r[2 * j], r[2 * j + 1]);
     epi_acquire(p, lane);
     epi_put_row(stage, lane, w);
-    epi_flush<KIND>(p, tmC, stage, lane, row0, col0);
+    epi_flush<KIND>(p, tmC, stage, lane, row0, col0, bz);
   }
 }
 
@@ -642,8 +652,9 @@ __global__ void __launch_bounds__(320, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        int mb, nb;
-        tile_coords(p, t, mb, nb);
+        int mb, nb, bz;
+        tile_coords(p, t, mb, nb, bz);
+        const int za = p.stride_a ? bz : 0, zb = p.stride_b ? bz : 0;  // a stride of 0 repeats matrix 0
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -653,15 +664,15 @@ __global__ void __launch_bounds__(320, 1)
           }
           const uint32_t fb = full0 + 8 * s;
           mbar_arrive_expect_tx(fb, tx);
-          if (p.a_tma) tma_load_2d(sA + s * Cf::A_BYTES, &tmA, fb, kb * Cf::BK, mb * Cf::BM);
+          if (p.a_tma) tma_load_3d(sA + s * Cf::A_BYTES, &tmA, fb, kb * Cf::BK, mb * Cf::BM, za);
           if (p.b_tma) {
             if constexpr (B_KMAJOR) {
-              tma_load_2d(sB + s * Cf::B_BYTES, &tmB, fb, kb * Cf::BK, nb * Cf::BN);
+              tma_load_3d(sB + s * Cf::B_BYTES, &tmB, fb, kb * Cf::BK, nb * Cf::BN, zb);
             } else {
 #pragma unroll
               for (int j = 0; j < Cf::NBOX; ++j)
-                tma_load_2d(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, nb * Cf::BN + j * Cf::BOXN,
-                            kb * Cf::BK);
+                tma_load_3d(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, nb * Cf::BN + j * Cf::BOXN,
+                            kb * Cf::BK, zb);
             }
           }
         }
@@ -714,8 +725,8 @@ __global__ void __launch_bounds__(320, 1)
     // ---------------------------------------------------------------- epilogue
     int tc = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tc) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
+      int mb, nb, bz;
+      tile_coords(p, t, mb, nb, bz);
       const int b = tc & 1;
       const uint32_t use = (tc >> 1) & 1;
       if (!warp_wait_phase(p, accf0 + 8 * b, use, ROLE_EPILOGUE | (b << 8))) break;
@@ -725,7 +736,7 @@ __global__ void __launch_bounds__(320, 1)
       const int ncols = min(Cf::BN, p.N - nb * Cf::BN);
       const uint32_t stage = sE + warp * EPI_WARP_BYTES;
       for_each_acc_chunk(taddr, (ncols + 31) / 32, [&](int c, const uint32_t(&r)[32]) {
-        emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, nb * Cf::BN + c * 32, r);
+        emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, nb * Cf::BN + c * 32, bz, r);
       });
       tc_fence_before();
       __syncwarp();
@@ -736,14 +747,14 @@ __global__ void __launch_bounds__(320, 1)
   } else {
     // ---------------------------------------------------------------- copy warps (6-9)
     const int ctid = threadIdx.x - 6 * 32;  // 0..127
-    const uint8_t* Ab = static_cast<const uint8_t*>(p.A);
-    const uint8_t* Bb = static_cast<const uint8_t*>(p.B);
     const long long lda_b = p.lda * Cf::ES, ldb_b = p.ldb * Cf::ES;
     int it = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
+      int mb, nb, bz;
+      tile_coords(p, t, mb, nb, bz);
+      const uint8_t* Ab = static_cast<const uint8_t*>(p.A) + bz * p.stride_a * Cf::ES;
+      const uint8_t* Bb = static_cast<const uint8_t*>(p.B) + bz * p.stride_b * Cf::ES;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = it % S;
         const uint32_t ph = (it / S) & 1;

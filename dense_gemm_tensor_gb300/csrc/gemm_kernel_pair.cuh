@@ -82,7 +82,7 @@ struct PairCfg {
 // Work item w of the pair kernel -> tile, k-slab range and (for split tiles)
 // the tail index f and segment.
 struct PairWork {
-  int mb, nb, kb0, kb1, f, seg;
+  int mb, nb, bz, kb0, kb1, f, seg;
 };
 __device__ __forceinline__ PairWork pair_work(const GemmParams& p, int w) {
   PairWork r;
@@ -99,7 +99,7 @@ __device__ __forceinline__ PairWork pair_work(const GemmParams& p, int w) {
     r.kb0 = static_cast<int>((static_cast<long long>(p.num_kb) * r.seg) / p.tail_segs);
     r.kb1 = static_cast<int>((static_cast<long long>(p.num_kb) * (r.seg + 1)) / p.tail_segs);
   }
-  tile_coords(p, t, r.mb, r.nb);
+  tile_coords(p, t, r.mb, r.nb, r.bz);
   return r;
 }
 
@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(192, 1)
         const PairWork wk = pair_work(p, w);
         const int row0 = wk.mb * Cf::BMP + int(half) * Cf::BM;
         const int col0 = (wk.nb * PAIRS + q) * BN + int(half) * Cf::BNH;
+        const int za = p.stride_a ? wk.bz : 0, zb = p.stride_b ? wk.bz : 0;  // a stride of 0 repeats matrix 0
         for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -210,19 +211,19 @@ __global__ void __launch_bounds__(192, 1)
           if (elect_one()) {
             if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_BYTES);
             if constexpr (PAIRS == 1) {
-              tma_load_2d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0);
+              tma_load_3d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0, za);
             } else {
               // both pairs need these 128 rows of A: each loads 64 of them into
               // the same place in its own and the other pair's CTA of this half
-              tma_load_2d_pair_mc(a_dst + q * (Cf::A_BYTES / 2), &tmA, fb, kb * Cf::BK, row0 + q * (Cf::BM / 2),
-                                  uint16_t(0x5u << half));
+              tma_load_3d_pair_mc(a_dst + q * (Cf::A_BYTES / 2), &tmA, fb, kb * Cf::BK, row0 + q * (Cf::BM / 2),
+                                  za, uint16_t(0x5u << half));
             }
             if constexpr (B_KMAJOR) {
-              tma_load_2d_pair(b_dst, &tmB, fb, kb * Cf::BK, col0);
+              tma_load_3d_pair(b_dst, &tmB, fb, kb * Cf::BK, col0, zb);
             } else {
 #pragma unroll
               for (int j = 0; j < Cf::NBOX; ++j)
-                tma_load_2d_pair(b_dst + j * Cf::BOX_BYTES, &tmB, fb, col0 + j * Cf::BOXN, kb * Cf::BK);
+                tma_load_3d_pair(b_dst + j * Cf::BOX_BYTES, &tmB, fb, col0 + j * Cf::BOXN, kb * Cf::BK, zb);
             }
           }
           __syncwarp();
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(192, 1)
       const int col0 = nbt * BN;
       if (wk.f < 0) {
         for_each_acc_chunk(taddr, nchunks,
-                           [&](int c, const uint32_t(&r)[32]) { emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, r); });
+                           [&](int c, const uint32_t(&r)[32]) { emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, wk.bz, r); });
       } else {
         // split tile: publish this segment's partial, then find out whether it is the last
         float4* mine = reinterpret_cast<float4*>(
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(192, 1)
               sum[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + cur[q].z);
               sum[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + cur[q].w);
             }
-            emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, sum);
+            emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, wk.bz, sum);
           });
         } else if (last) {
           // three or four segments: add them in segment order; this CTA's own one comes from tensor memory
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t out[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) out[j] = __float_as_uint(acc[j]);
-            emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, out);
+            emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, wk.bz, out);
           });
         }
       }

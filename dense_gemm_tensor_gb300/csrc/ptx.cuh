@@ -73,22 +73,25 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// 2-D tiled load of one box into shared memory; completion is signalled as
-// transaction bytes on `bar`. Coordinates are in elements, x innermost.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int32_t x,
-                                            int32_t y) {
+// The tensor maps are 3-D: (x innermost, y rows, z matrix of a batch; z = 0
+// for a single product). Coordinates are in elements.
+
+// Tiled load of one box into shared memory; completion is signalled as
+// transaction bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int32_t x, int32_t y,
+                                            int32_t z) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 
-// 2-D tiled store of one box from shared memory to global memory, tracked by
-// the issuing thread's bulk async-groups. Parts of the box outside the tensor
-// are not written.
-__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
-               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(x), "r"(y)
+// Tiled store of one box from shared memory to global memory, tracked by the
+// issuing thread's bulk async-groups. Parts of the box outside the tensor are
+// not written.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -212,12 +215,12 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 
 // 2-D tiled TMA load into this CTA's shared memory whose completion is
 // signalled on an mbarrier of either CTA of the pair (shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t x,
-                                                 int32_t y) {
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t x,
+                                                 int32_t y, int32_t z) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
-      "[%0], [%1, {%3, %4}], [%2];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%3, %4, %5}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 
@@ -265,16 +268,16 @@ __device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d, uint64_t a, uint64_t
 
 // Arrive once on the mbarrier at CTA-local offset `bar` in every CTA of
 // `cta_mask` when this thread's earlier pair MMAs have completed.
-// 2-D tiled TMA load multicast to the CTAs of `cta_mask` (the data lands at
+// Tiled TMA load multicast to the CTAs of `cta_mask` (the data lands at
 // offset `dst` of each). With .cta_group::2 each destination's completion is
 // signalled on the barrier at the offset of `bar_cluster` in the leader (even
 // rank) CTA of that destination's pair, so `bar_cluster` names a leader's barrier.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t x,
-                                                    int32_t y, uint16_t cta_mask) {
+__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t x,
+                                                    int32_t y, int32_t z, uint16_t cta_mask) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "h"(cta_mask)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".cta_group::2 [%0], [%1, {%3, %4, %5}], [%2], %6;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
       : "memory");
 }
 

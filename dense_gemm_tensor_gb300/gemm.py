@@ -48,7 +48,8 @@ class Epilogue(ctypes.Structure):
 EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_tf32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_e4m3", "gemm_e5m2",
            "gemm_status_string", "gemm_get_device_status", "gemm_reset_device_status", "gemm_set_debug",
            "gemm_launch_count", "gemm_set_tuning", "gemm_last_plan", "gemm_free_workspaces",
-           "gemm_bf16_static_scratch")
+           "gemm_bf16_static_scratch", "gemm_tf32_strided_batched", "gemm_f16_strided_batched",
+           "gemm_bf16_strided_batched")
 
 _lib = None
 
@@ -76,6 +77,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     for name in ("gemm_tf32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_e4m3", "gemm_e5m2"):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, ctypes.POINTER(Epilogue), vp]
+        fn.restype = ctypes.c_int
+    for name in ("gemm_tf32_strided_batched", "gemm_f16_strided_batched", "gemm_bf16_strided_batched"):
+        fn = getattr(lib, name)
+        fn.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64, ctypes.c_int,
+                       ctypes.POINTER(Epilogue), vp]
         fn.restype = ctypes.c_int
     lib.gemm_status_string.argtypes = [ctypes.c_int]
     lib.gemm_status_string.restype = ctypes.c_char_p
@@ -250,6 +256,47 @@ def _matmul_fp8(A, B, out, layout, stream, alpha, beta, bias, activation):
               out.data_ptr() or None, _rows(out, "out"), layout, ctypes.byref(epi), s)
     if code != GEMM_OK:
         raise GemmError(code, _FP8[dt])
+    return out
+
+
+def bmm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, layout: int = GEMM_B_ROW_MAJOR,
+        stream: torch.cuda.Stream | None = None, alpha: float = 1.0, beta: float = 0.0,
+        bias: torch.Tensor | None = None, activation: str | None = None) -> torch.Tensor:
+    """Strided batch C[z] = A[z] . B[z] (gemm_*_strided_batched), optionally
+    with the fused epilogue. A: batch x M x K; B: batch x K x N (layout 0) or
+    batch x N x K (layout 1); a batch stride of 0 (``expand``) repeats one
+    matrix. Rows must be contiguous; the other strides come from the tensors."""
+    dt = A.dtype
+    if dt not in _BY_DTYPE or B.dtype != dt:
+        raise TypeError("A and B must both be float32, float16 or bfloat16")
+    if A.dim() != 3 or B.dim() != 3 or A.shape[0] != B.shape[0]:
+        raise ValueError("A and B must be 3-D with the same batch size")
+    batch, M, K = A.shape
+    N = B.shape[2] if layout == GEMM_B_ROW_MAJOR else B.shape[1]
+    if (B.shape[1] if layout == GEMM_B_ROW_MAJOR else B.shape[2]) != K:
+        raise ValueError("B's K dimension does not match A")
+    if out is None:
+        out = torch.empty((batch, M, N), dtype=dt, device=A.device)
+    elif out.dtype != dt or tuple(out.shape) != (batch, M, N):
+        raise ValueError("out must be batch x M x N with the operands' dtype")
+    for t, what in ((A, "A"), (B, "B"), (out, "out")):
+        if t.shape[2] > 1 and t.stride(2) != 1:
+            raise ValueError(f"{what} must have unit stride along its rows")
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(k for k in ACTIVATIONS if k)}")
+    if bias is not None and (bias.dtype != dt or bias.dim() != 1 or bias.numel() != N or not bias.is_cuda or
+                             (N > 1 and bias.stride(0) != 1)):
+        raise ValueError("bias must be a contiguous CUDA vector of N elements of the operands' dtype")
+    epi = Epilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None, ACTIVATIONS[activation])
+    s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    ld = lambda t: t.stride(1) if t.shape[1] > 1 else t.shape[2]  # noqa: E731
+    bs = lambda t: t.stride(0) if t.shape[0] > 1 else 0  # noqa: E731
+    name = _BY_DTYPE[dt] + "_strided_batched"
+    code = getattr(load(), name)(batch, M, N, K, A.data_ptr() or None, ld(A), bs(A), B.data_ptr() or None, ld(B),
+                                 bs(B), out.data_ptr() or None, ld(out), bs(out) if batch > 1 else 0, layout,
+                                 ctypes.byref(epi), s)
+    if code != GEMM_OK:
+        raise GemmError(code, name)
     return out
 
 

@@ -144,6 +144,33 @@ int gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda
                  uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream);
 
 /*
+ * Strided batches: for z = 0 .. batch-1,
+ *   C_z = A_z . B_z  (with the fused epilogue when `epilogue` is not NULL),
+ * where X_z starts stride_x elements after X_{z-1} (X = A, B, C); a stride of
+ * 0 for A or B uses the same matrix for every z (e.g. one weight matrix), and
+ * the bias, if any, is shared by the whole batch. Each matrix has the layout,
+ * leading dimension and rules of the single product above. One launch covers
+ * the whole batch: the output tiles of every matrix are spread over the GPU
+ * together (matrix by matrix in tile order), so many small products fill it.
+ * Additional rules: batch >= 0 (0 does nothing); stride_c >= (M-1)*ldc + N so
+ * the C matrices do not overlap, and a nonzero stride_a / stride_b at least
+ * one matrix's extent; for batch > 1 the rows and matrix strides of A and B
+ * must be 16-byte multiples with 16-byte-aligned bases (GEMM_ERR_MISALIGNED
+ * otherwise), and C must not overlap any A or B of the batch. Strides are
+ * below 2^40 elements; batch times the 128 x 128 tiles of one matrix below 2^31.
+ */
+int gemm_tf32_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                              int64_t stride_a, const float* B, int64_t ldb, int64_t stride_b, float* C, int64_t ldc,
+                              int64_t stride_c, int layout, const gemm_epilogue_t* epilogue, void* stream);
+int gemm_f16_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                             int64_t stride_a, const uint16_t* B, int64_t ldb, int64_t stride_b, uint16_t* C,
+                             int64_t ldc, int64_t stride_c, int layout, const gemm_epilogue_t* epilogue, void* stream);
+int gemm_bf16_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                              int64_t stride_a, const uint16_t* B, int64_t ldb, int64_t stride_b, uint16_t* C,
+                              int64_t ldc, int64_t stride_c, int layout, const gemm_epilogue_t* epilogue,
+                              void* stream);
+
+/*
  * FP8 products: A and B hold OCP FP8 bytes -- E4M3 (gemm_e4m3: 1 sign, 4
  * exponent bits with bias 7, 3 mantissa bits; no infinities, S.1111.111 is
  * NaN; largest finite 448) or E5M2 (gemm_e5m2: 1 sign, 5 exponent bits with
