@@ -677,8 +677,15 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
       ok = encode_3d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, zb, uint64_t(p.stride_b) * es, bk,
                      uint32_t(plan.pair ? bn / 2 : bn));
     } else {
+      const CUtensorMapSwizzle swz = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
       ok = encode_3d(&L.tmB, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, zb, uint64_t(p.stride_b) * es,
-                     128 / es, bk, es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
+                     128 / es, bk, swz);
+      // the last box of a tile whose columns per CTA are not whole 128-byte boxes
+      const int cols = plan.pair ? bn / 2 : bn, boxn = 128 / es;
+      const int lastn = cols - (cols + boxn - 1) / boxn * boxn + boxn;
+      if (ok && lastn != boxn)
+        ok = encode_3d(&L.tmB2, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, zb, uint64_t(p.stride_b) * es,
+                       uint32_t(lastn), bk, swz);
     }
     if (!ok) return GEMM_ERR_DRIVER;
   }

@@ -173,6 +173,9 @@ struct Cfg {
   static constexpr int NBOX = (BN + BOXN - 1) / BOXN;  // MN-major B: boxes per stage (last may be partly used)
   static constexpr int BOX_BYTES = BK * 128;
   static constexpr int B_BYTES = B_KMAJOR ? BN * 128 : NBOX * BOX_BYTES;
+  // MN-major B: the last box carries only the tile's columns (see the pair kernel)
+  static constexpr int LASTN = BN - (NBOX - 1) * BOXN;
+  static constexpr int B_TX = B_KMAJOR ? B_BYTES : (NBOX - 1) * BOX_BYTES + LASTN * BK * ES;
   // MN-major B of 32-bit elements uses the 128-byte swizzle with 32-byte
   // atoms (16-bit MN-major and every K-major tile use 16-byte atoms).
   static constexpr bool B_ATOM32 = (ES == 4) && !B_KMAJOR;
@@ -594,7 +597,8 @@ __device__ __forceinline__ void for_each_acc_chunk(uint32_t taddr, int nchunks, 
 template <int KIND, bool B_KMAJOR, int BN>
 __global__ void __launch_bounds__(320, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
+                const GemmParams p) {
   using Cf = Cfg<KIND, B_KMAJOR, BN>;
   constexpr int S = Cf::STAGES;
 
@@ -635,6 +639,7 @@ __global__ void __launch_bounds__(320, 1)
     fence_mbar_init();
     if (p.a_tma) tma_prefetch_desc(&tmA);
     if (p.b_tma) tma_prefetch_desc(&tmB);
+    if (p.b_tma && !B_KMAJOR && Cf::LASTN != Cf::BOXN) tma_prefetch_desc(&tmB2);
   }
   if (warp == 5) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), Cf::TMEM_COLS);
@@ -648,7 +653,7 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 4) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && !(p.debug & DEBUG_STALL_PRODUCER)) {
-      const uint32_t tx = (p.a_tma ? Cf::A_BYTES : 0) + (p.b_tma ? Cf::B_BYTES : 0);
+      const uint32_t tx = (p.a_tma ? Cf::A_BYTES : 0) + (p.b_tma ? Cf::B_TX : 0);
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
@@ -671,8 +676,9 @@ __global__ void __launch_bounds__(320, 1)
             } else {
 #pragma unroll
               for (int j = 0; j < Cf::NBOX; ++j)
-                tma_load_3d(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES, &tmB, fb, nb * Cf::BN + j * Cf::BOXN,
-                            kb * Cf::BK, zb);
+                tma_load_3d(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES,
+                            (j == Cf::NBOX - 1 && Cf::LASTN != Cf::BOXN) ? &tmB2 : &tmB, fb,
+                            nb * Cf::BN + j * Cf::BOXN, kb * Cf::BK, zb);
             }
           }
         }

@@ -54,10 +54,16 @@ struct PairCfg {
   static constexpr int NBOX = (BNH + BOXN - 1) / BOXN;  // MN-major B: boxes per CTA (last may be partly used)
   static constexpr int BOX_BYTES = BK * 128;
   static constexpr int B_BYTES = B_KMAJOR ? BNH * 128 : NBOX * BOX_BYTES;
+  // MN-major B: the last box carries only the columns the tile uses (a
+  // narrower box still lands in 128-byte swizzled rows), so a stage moves
+  // B_TX bytes of B while taking B_BYTES of shared memory.
+  static constexpr int LASTN = BNH - (NBOX - 1) * BOXN;
+  static constexpr int B_TX = B_KMAJOR ? B_BYTES : (NBOX - 1) * BOX_BYTES + LASTN * BK * ES;
   static constexpr bool B_ATOM32 = (ES == 4) && !B_KMAJOR;
   static constexpr uint32_t B_SWZ = B_ATOM32 ? SWZ_128B_ATOM32 : SWZ_128B;
   static constexpr uint32_t B_SBO = B_ATOM32 ? DGT_ATOM32_SBO : 1024;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGE_TX = A_BYTES + B_TX;  // bytes the TMA loads of one CTA's stage deliver
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int RESERVED = 1024 /*align slack*/ + EPI_BYTES /*output staging*/ + 256 /*barriers*/;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED) / STAGE_BYTES;
@@ -124,7 +130,8 @@ __device__ __forceinline__ void epilogue_barrier() { asm volatile("bar.sync 1, 1
 template <int KIND, bool B_KMAJOR, int BN, int PAIRS>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
+                     const GemmParams p) {
   using Cf = PairCfg<KIND, B_KMAJOR, BN>;
   constexpr int S = Cf::STAGES;
   constexpr int NB = Cf::ACC_BUFS;
@@ -175,6 +182,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (!B_KMAJOR && Cf::LASTN != Cf::BOXN) tma_prefetch_desc(&tmB2);
   }
   if (warp == 5) {
     tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), Cf::TMEM_COLS);
@@ -209,7 +217,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t a_dst = sA + s * Cf::A_BYTES;
           const uint32_t b_dst = sB + s * Cf::B_BYTES;
           if (elect_one()) {
-            if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_BYTES);
+            if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_TX);
             if constexpr (PAIRS == 1) {
               tma_load_3d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0, za);
             } else {
@@ -223,7 +231,8 @@ __global__ void __launch_bounds__(192, 1)
             } else {
 #pragma unroll
               for (int j = 0; j < Cf::NBOX; ++j)
-                tma_load_3d_pair(b_dst + j * Cf::BOX_BYTES, &tmB, fb, col0 + j * Cf::BOXN, kb * Cf::BK, zb);
+                tma_load_3d_pair(b_dst + j * Cf::BOX_BYTES, (j == Cf::NBOX - 1 && Cf::LASTN != Cf::BOXN) ? &tmB2 : &tmB,
+                                 fb, col0 + j * Cf::BOXN, kb * Cf::BK, zb);
             }
           }
           __syncwarp();

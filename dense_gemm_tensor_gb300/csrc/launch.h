@@ -12,6 +12,7 @@ namespace dgt {
 struct LaunchPlan {
   CUtensorMap tmA;  // valid when p.a_tma
   CUtensorMap tmB;  // valid when p.b_tma
+  CUtensorMap tmB2; // MN-major B whose tile columns are not whole 128-byte boxes: the last, narrower box
   CUtensorMap tmC;  // valid when p.c_tma
   GemmParams p;
   bool b_kmajor;
@@ -86,7 +87,7 @@ cudaError_t launch_variant(const LaunchPlan& L) {
     if (e != cudaSuccess) return e;
     if (dev < 64) __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
   }
-  kern<<<L.grid, L.threads, smem, L.stream>>>(L.tmA, L.tmB, L.tmC, L.p);
+  kern<<<L.grid, L.threads, smem, L.stream>>>(L.tmA, L.tmB, L.tmB2, L.tmC, L.p);
   return cudaGetLastError();
 }
 
@@ -127,7 +128,7 @@ cudaError_t launch_pair_variant(const LaunchPlan& L) {
   cfg.stream = L.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmC, L.p);
+  e = cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmB2, L.tmC, L.p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
