@@ -155,9 +155,23 @@ struct GemmParams {
   const void* bias;
 };
 
-// Output staging in shared memory: 2 KB per epilogue warp (see epi_chunk_addr).
+// Output staging in shared memory (see epi_chunk_addr): each epilogue warp
+// has a ring of 1-4 tiles of 2 KB (EPI_BYTES = one tile for each of the four
+// warps); the shared memory the operand stages leave over sets the count.
 constexpr int EPI_WARP_BYTES = 32 * 64;
 constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+
+// Staging tiles needed per warp, given what a kernel's stages leave of `limit`.
+constexpr int epi_bufs_for(int limit, int used) {
+  return (limit - used) / EPI_BYTES >= 4 ? 4 : (limit - used) / EPI_BYTES < 1 ? 1 : (limit - used) / EPI_BYTES;
+}
+
+// A warp's staging ring: round i writes tile i mod bufs.
+struct EpiRing {
+  uint32_t base;  // this warp's first tile
+  int bufs;
+  int next;
+};
 
 template <int KIND, bool B_KMAJOR, int BN_>
 struct Cfg {
@@ -183,9 +197,10 @@ struct Cfg {
   static constexpr uint32_t B_SBO = B_ATOM32 ? DGT_ATOM32_SBO : 1024;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SMEM_LIMIT = 232448;  // opt-in dynamic shared memory per block
-  static constexpr int RESERVED = 1024 /*align slack*/ + EPI_BYTES /*output staging*/ + 256 /*barriers*/;
-  static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED) / STAGE_BYTES;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - (1024 + EPI_BYTES + 256)) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int EPI_BUFS = epi_bufs_for(SMEM_LIMIT, 1024 + 256 + STAGES * STAGE_BYTES);
+  static constexpr int RESERVED = 1024 /*align slack*/ + EPI_BUFS * EPI_BYTES /*output staging*/ + 256 /*barriers*/;
   static constexpr int ACC_COLS = BN;       // fp32 accumulator columns of one buffer
   static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // power of two >= 2 * BN
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
@@ -373,11 +388,22 @@ __device__ __forceinline__ uint32_t epi_chunk_addr(uint32_t stage, int r, int j)
   return stage + static_cast<uint32_t>(r * 64) + (static_cast<uint32_t>(j ^ ((r >> 1) & 3)) << 4);
 }
 
-// The tile may be overwritten once the previous round's TMA store has read it
-// (only lane 0 has stores in flight).
-__device__ __forceinline__ void epi_acquire(const GemmParams& p, int lane) {
-  if (p.c_tma && lane == 0) bulk_wait_read_all();
+// The next tile of the warp's ring, once the TMA store that last used it has
+// read it (only lane 0 has stores in flight; up to bufs - 1 younger ones may
+// still be reading their tiles).
+__device__ __forceinline__ uint32_t epi_acquire(const GemmParams& p, int lane, EpiRing& ring) {
+  const uint32_t stage = ring.base + static_cast<uint32_t>(ring.next % ring.bufs) * EPI_WARP_BYTES;
+  ++ring.next;
+  if (p.c_tma && lane == 0) {
+    switch (ring.bufs) {
+      case 1: bulk_wait_read<0>(); break;
+      case 2: bulk_wait_read<1>(); break;
+      case 3: bulk_wait_read<2>(); break;
+      default: bulk_wait_read<3>(); break;
+    }
+  }
   __syncwarp();
+  return stage;
 }
 
 __device__ __forceinline__ void epi_put_row(uint32_t stage, int lane, const uint32_t (&w)[16]) {
@@ -491,11 +517,11 @@ __device__ __forceinline__ float epi_activation(float v, int act) {
 // in fp32, then rounded to the output type. The round's accumulator columns
 // are r[OFF .. OFF + 63 / ES] (32 for 16-bit C, 16 for fp32 C).
 template <int KIND, int OFF>
-__device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage,
+__device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUtensorMap* tmC, EpiRing& ring,
                                                 int lane, int row0, int col0, int bz, const uint32_t (&r)[32]) {
   constexpr int RC = KIND == KIND_TF32 ? 16 : 32;
   using T = typename KindTraits<KIND>::T;
-  epi_acquire(p, lane);
+  const uint32_t stage = epi_acquire(p, lane, ring);
   float v[RC];
 #pragma unroll
   for (int k = 0; k < RC; ++k) v[k] = p.alpha * __uint_as_float(r[OFF + k]);
@@ -539,11 +565,11 @@ __device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUten
 // matrix bz, through the fused epilogue when the launch has one.
 // Warp-collective.
 template <int KIND>
-__device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMap* tmC, uint32_t stage, int lane,
+__device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMap* tmC, EpiRing& ring, int lane,
                                            int row0, int col0, int bz, const uint32_t (&r)[32]) {
   if (p.fused) {
-    epi_round_fused<KIND, 0>(p, tmC, stage, lane, row0, col0, bz, r);
-    if (KIND == KIND_TF32 && col0 + 16 < p.N) epi_round_fused<KIND, 16>(p, tmC, stage, lane, row0, col0 + 16, bz, r);
+    epi_round_fused<KIND, 0>(p, tmC, ring, lane, row0, col0, bz, r);
+    if (KIND == KIND_TF32 && col0 + 16 < p.N) epi_round_fused<KIND, 16>(p, tmC, ring, lane, row0, col0 + 16, bz, r);
     return;
   }
   if constexpr (KIND == KIND_TF32) {
@@ -553,7 +579,7 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
       uint32_t w[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) w[j] = r[16 * h + j];
-      epi_acquire(p, lane);
+      const uint32_t stage = epi_acquire(p, lane, ring);
       epi_put_row(stage, lane, w);
       epi_flush<KIND>(p, tmC, stage, lane, row0, col0 + 16 * h, bz);
     }
@@ -561,7 +587,7 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
     uint32_t w[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) w[j] = pack2<KIND>(r[2 * j], r[2 * j + 1]);
-    epi_acquire(p, lane);
+    const uint32_t stage = epi_acquire(p, lane, ring);
     epi_put_row(stage, lane, w);
     epi_flush<KIND>(p, tmC, stage, lane, row0, col0, bz);
   }
@@ -608,8 +634,8 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sptr = smem_raw + (sbase - raw);
   const uint32_t sA = sbase;
   const uint32_t sB = sbase + S * Cf::A_BYTES;
-  const uint32_t sE = sbase + S * (Cf::A_BYTES + Cf::B_BYTES);  // output staging, EPI_BYTES
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sptr + S * (Cf::A_BYTES + Cf::B_BYTES) + EPI_BYTES);
+  const uint32_t sE = sbase + S * (Cf::A_BYTES + Cf::B_BYTES);  // output staging, EPI_BUFS x EPI_BYTES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sptr + S * (Cf::A_BYTES + Cf::B_BYTES) + Cf::EPI_BUFS * EPI_BYTES);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
   const uint32_t accf0 = empty0 + 8 * S;
@@ -730,6 +756,7 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue
     int tc = 0;
+    EpiRing ring{sE + static_cast<uint32_t>(warp * Cf::EPI_BUFS * EPI_WARP_BYTES), Cf::EPI_BUFS, 0};
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tc) {
       int mb, nb, bz;
       tile_coords(p, t, mb, nb, bz);
@@ -740,9 +767,8 @@ __global__ void __launch_bounds__(320, 1)
       const int row0 = mb * Cf::BM + warp * 32;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
       const int ncols = min(Cf::BN, p.N - nb * Cf::BN);
-      const uint32_t stage = sE + warp * EPI_WARP_BYTES;
       for_each_acc_chunk(taddr, (ncols + 31) / 32, [&](int c, const uint32_t(&r)[32]) {
-        emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, nb * Cf::BN + c * 32, bz, r);
+        emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, nb * Cf::BN + c * 32, bz, r);
       });
       tc_fence_before();
       __syncwarp();

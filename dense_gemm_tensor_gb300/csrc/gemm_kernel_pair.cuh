@@ -65,9 +65,10 @@ struct PairCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGE_TX = A_BYTES + B_TX;  // bytes the TMA loads of one CTA's stage deliver
   static constexpr int SMEM_LIMIT = 232448;
-  static constexpr int RESERVED = 1024 /*align slack*/ + EPI_BYTES /*output staging*/ + 256 /*barriers*/;
-  static constexpr int STAGES_FIT = (SMEM_LIMIT - RESERVED) / STAGE_BYTES;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - (1024 + EPI_BYTES + 256)) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int EPI_BUFS = epi_bufs_for(SMEM_LIMIT, 1024 + 256 + STAGES * STAGE_BYTES);
+  static constexpr int RESERVED = 1024 /*align slack*/ + EPI_BUFS * EPI_BYTES /*output staging*/ + 256 /*barriers*/;
   static constexpr int ACC_BUFS = 2;  // the epilogue of one tile overlaps the next tile's k-loop
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = (ACC_BUFS * BN <= 256) ? 256 : 512;
@@ -144,8 +145,8 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sptr = smem_raw + (sbase - raw);
   const uint32_t sA = sbase;
   const uint32_t sB = sbase + S * Cf::A_BYTES;
-  const uint32_t sE = sbase + S * Cf::STAGE_BYTES;  // output staging, EPI_BYTES
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sptr + S * Cf::STAGE_BYTES + EPI_BYTES);
+  const uint32_t sE = sbase + S * Cf::STAGE_BYTES;  // output staging, EPI_BUFS x EPI_BYTES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sptr + S * Cf::STAGE_BYTES + Cf::EPI_BUFS * EPI_BYTES);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S;
   const uint32_t accf0 = empty0 + 8 * S;
@@ -301,6 +302,7 @@ __global__ void __launch_bounds__(192, 1)
     // barrier publishes the outcome), so the barriers below always see all 128.
     const int tid = threadIdx.x;  // 0..127
     int tc = 0;
+    EpiRing ring{sE + static_cast<uint32_t>(warp * Cf::EPI_BUFS * EPI_WARP_BYTES), Cf::EPI_BUFS, 0};
     for (int w = pair; w < p.num_work; w += npairs, ++tc) {
       const PairWork wk = pair_work(p, w);
       const int b = tc % NB;
@@ -311,14 +313,13 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const int nbt = wk.nb * PAIRS + q;  // this pair's tile column (past the last one: nothing to store)
       const int row0 = wk.mb * Cf::BMP + int(half) * Cf::BM + warp * 32;  // first of this warp's 32 rows
-      const uint32_t stage = sE + warp * EPI_WARP_BYTES;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
       const int ncols = min(BN, p.N - nbt * BN);
       const int nchunks = ncols > 0 ? (ncols + 31) / 32 : 0;
       const int col0 = nbt * BN;
       if (wk.f < 0) {
         for_each_acc_chunk(taddr, nchunks,
-                           [&](int c, const uint32_t(&r)[32]) { emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, wk.bz, r); });
+                           [&](int c, const uint32_t(&r)[32]) { emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, r); });
       } else {
         // split tile: publish this segment's partial, then find out whether it is the last
         float4* mine = reinterpret_cast<float4*>(
@@ -362,7 +363,7 @@ __global__ void __launch_bounds__(192, 1)
               sum[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + cur[q].z);
               sum[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + cur[q].w);
             }
-            emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, wk.bz, sum);
+            emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, sum);
           });
         } else if (last) {
           // three or four segments: add them in segment order; this CTA's own one comes from tensor memory
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t out[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) out[j] = __float_as_uint(acc[j]);
-            emit_chunk<KindTraits<KIND>::out>(p, &tmC, stage, lane, row0, col0 + c * 32, wk.bz, out);
+            emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, out);
           });
         }
       }
