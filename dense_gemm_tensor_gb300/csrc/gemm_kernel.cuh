@@ -774,7 +774,9 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * b);
     }
-    if (lane == 0) bulk_wait_all();  // this warp's TMA stores of C have completed
+    // this warp's TMA stores of C have read their staging tiles (the shared
+    // memory may be released; the grid's completion covers their writes)
+    if (lane == 0) bulk_wait_read_all();
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- copy warps (6-9)

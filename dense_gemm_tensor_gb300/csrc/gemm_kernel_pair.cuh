@@ -400,7 +400,9 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(acce0 + 8 * b, lead));
     }
-    if (lane == 0) bulk_wait_all();  // this warp's TMA stores of C have completed
+    // this warp's TMA stores of C have read their staging tiles (the shared
+    // memory may be released; the grid's completion covers their writes)
+    if (lane == 0) bulk_wait_read_all();
     __syncwarp();
   }
 
