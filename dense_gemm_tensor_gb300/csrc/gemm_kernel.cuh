@@ -675,6 +675,8 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // set-up done; from here on A, B, C and the scratch are read or written
+  grid_dependency_wait();
 
   if (warp == 4) {
     // ---------------------------------------------------------------- TMA producer
@@ -711,6 +713,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       *issued_slot = it;
     }
+    grid_launch_dependents();  // this CTA's last operand load is issued
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {

@@ -194,6 +194,8 @@ __global__ void __launch_bounds__(192, 1)
   cluster_sync();  // barriers of both CTAs initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // set-up done; from here on A, B, C and the scratch are read or written
+  grid_dependency_wait();
 
   if (warp == 4) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
@@ -241,6 +243,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (lane == 0) *issued_slot = it;
     }
+    grid_launch_dependents();  // this CTA's last operand load is issued
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer (leader only)
     // The whole warp walks the loop and builds the descriptors (warp-uniform);

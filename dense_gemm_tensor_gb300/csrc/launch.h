@@ -87,7 +87,18 @@ cudaError_t launch_variant(const LaunchPlan& L) {
     if (e != cudaSuccess) return e;
     if (dev < 64) __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
   }
-  kern<<<L.grid, L.threads, smem, L.stream>>>(L.tmA, L.tmB, L.tmB2, L.tmC, L.p);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pair_variant
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(L.grid, 1, 1);
+  cfg.blockDim = dim3(L.threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmB2, L.tmC, L.p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -117,17 +128,22 @@ cudaError_t launch_pair_variant(const LaunchPlan& L) {
     if (dev < 64) __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2 * PAIRS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch: the kernel may be scheduled while the
+  // previous kernel on the stream finishes; it runs its set-up, then waits
+  // (griddepcontrol.wait) for that kernel to complete before touching memory.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(L.grid, 1, 1);
   cfg.blockDim = dim3(L.threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmB2, L.tmC, L.p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
