@@ -339,6 +339,9 @@ constexpr double kSlabCycles[3][4] = {
     {564.0, 504.0, 499.0, 464.0},  // CTA pair, 256 x width tiles
     {560.0, 503.0, 500.0, 470.0},  // two pairs sharing A, two 256 x width tiles
 };
+// TF32 with row-major B fetches B in 32-column boxes, twice as many as the
+// 16-bit kinds; its pair and shared-A slabs measured 564/542/495/476 cycles.
+constexpr double kSlabCyclesTf32Mn[4] = {564.0, 542.0, 495.0, 476.0};
 
 // Picks the kernel (single CTA, CTA pair, or two pairs sharing A), the tile
 // width and the tile order.
@@ -370,7 +373,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
       conc = sms;
     }
     const int wi = bn == 256 ? 0 : bn == 224 ? 1 : bn == 192 ? 2 : 3;
-    const double slab = kSlabCycles[pair ? pairs : 0][wi];
+    const double slab = (pair && kind == KIND_TF32 && !kmajor) ? kSlabCyclesTf32Mn[wi] : kSlabCycles[pair ? pairs : 0][wi];
     const int64_t rows = pair ? 256 : 128;
     const int64_t tiles_n = (N + bn - 1) / bn;
     const int64_t tiles = nbat * ((M + rows - 1) / rows) * ((tiles_n + pairs - 1) / pairs);
