@@ -302,32 +302,61 @@ def bmm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, la
 
 def matmul_from_host(A_host: torch.Tensor, B_host: torch.Tensor, *, layout: int = GEMM_B_ROW_MAJOR,
                      device: torch.device | str = "cuda", stream: torch.cuda.Stream | None = None,
-                     buffers: dict | None = None) -> torch.Tensor:
+                     buffers: dict | None = None, chunks: int | None = None) -> torch.Tensor:
     """End-to-end product of host operands: copy A and B to the device, run
-    the kernel, copy C back into a pinned host tensor, and synchronise.
+    the kernels, copy C back into a pinned host tensor, and synchronise.
 
-    ``buffers`` (optional, reused across calls) caches the device and pinned
-    host buffers so repeated calls do not allocate.
+    B is copied first; A is then streamed in row blocks: block i's product
+    runs while block i+1 is copied in and block i-1's rows of C are copied out
+    (three streams, ordered by events), so the host<->device copies in both
+    directions overlap each other and the kernels. ``chunks`` sets the number
+    of row blocks (default: one per 1024 rows of A, at most 4). ``buffers``
+    (optional, reused across calls) caches the device and pinned host buffers,
+    streams and events so repeated calls do not allocate.
     """
     buffers = {} if buffers is None else buffers
     dev = torch.device(device)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    M = A_host.shape[0]
+    N = B_host.shape[1] if layout == GEMM_B_ROW_MAJOR else B_host.shape[0]
+    out_dtype = torch.bfloat16 if A_host.dtype in _FP8 else A_host.dtype
     key = (A_host.shape, B_host.shape, A_host.dtype, layout)
     if buffers.get("key") != key:
-        M = A_host.shape[0]
-        N = B_host.shape[1] if layout == GEMM_B_ROW_MAJOR else B_host.shape[0]
         buffers.update(key=key,
                        a=torch.empty(A_host.shape, dtype=A_host.dtype, device=dev),
                        b=torch.empty(B_host.shape, dtype=B_host.dtype, device=dev),
-                       c=torch.empty((M, N), dtype=A_host.dtype, device=dev),
-                       c_host=torch.empty((M, N), dtype=A_host.dtype, pin_memory=True))
-    with torch.cuda.stream(s):
-        buffers["a"].copy_(A_host, non_blocking=True)
-        buffers["b"].copy_(B_host, non_blocking=True)
-        matmul(buffers["a"], buffers["b"], buffers["c"], layout=layout, stream=s)
-        buffers["c_host"].copy_(buffers["c"], non_blocking=True)
+                       c=torch.empty((M, N), dtype=out_dtype, device=dev),
+                       c_host=torch.empty((M, N), dtype=out_dtype, pin_memory=True),
+                       s_in=torch.cuda.Stream(dev), s_out=torch.cuda.Stream(dev))
+    n = chunks if chunks is not None else max(1, min(4, M // 1024))
+    n = max(1, min(n, M)) if M > 0 else 1
+    bounds = [M * i // n for i in range(n + 1)]
+    a, b, c, c_host = buffers["a"], buffers["b"], buffers["c"], buffers["c_host"]
+    s_in, s_out = buffers["s_in"], buffers["s_out"]
+    start = torch.cuda.Event()
+    start.record(s)
+    s_in.wait_event(start)
+    s_out.wait_event(start)
+    with torch.cuda.stream(s_in):
+        b.copy_(B_host, non_blocking=True)
+    for i in range(n):
+        lo, hi = bounds[i], bounds[i + 1]
+        with torch.cuda.stream(s_in):
+            a[lo:hi].copy_(A_host[lo:hi], non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(s_in)
+        s.wait_event(arrived)
+        with torch.cuda.stream(s):
+            if hi > lo:
+                matmul(a[lo:hi], b, c[lo:hi], layout=layout, stream=s)
+            computed = torch.cuda.Event()
+            computed.record(s)
+        s_out.wait_event(computed)
+        with torch.cuda.stream(s_out):
+            c_host[lo:hi].copy_(c[lo:hi], non_blocking=True)
+    s_out.synchronize()
     s.synchronize()
-    return buffers["c_host"]
+    return c_host
 
 
 def device_status(stream: torch.cuda.Stream | None = None) -> int:

@@ -296,3 +296,15 @@ def test_workload_sampled(name):
     C, _ = _run(p)
     res = _check_sampled(p, C, 3000 + n)
     print(name, res)
+
+
+@pytest.mark.parametrize("dtype,layout,chunks", [("bf16", 0, None), ("tf32", 1, 3), ("f16", 0, 1)])
+def test_matmul_from_host_pipelined(dtype, layout, chunks):
+    """The end-to-end call on pinned host operands: row blocks of A streamed in,
+    blocks of C streamed out while the next block computes; every entry checked."""
+    M, N, K = 2600, 700, 900
+    p = inputs.make_problem("host", dtype, M, N, K, layout=layout, seed_a=61, seed_b=62)
+    bufs = {}
+    for _ in range(2):  # the second call reuses the cached buffers and streams
+        C = gemm.matmul_from_host(p.a.pin_memory(), p.b.pin_memory(), layout=layout, buffers=bufs, chunks=chunks)
+    _check_full(p, C)
