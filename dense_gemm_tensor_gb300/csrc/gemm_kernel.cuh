@@ -5,20 +5,25 @@
 // with operands staged through shared memory, a pipelined k-loop, tensor-core
 // MMA with fp32 accumulation, grid-swizzled tile order for L2 reuse, and an
 // epilogue that converts the fp32 accumulator to the output type with
-// round-to-nearest-even. Here each of those steps is a Blackwell unit:
+// round-to-nearest-even. Here each of those steps is a Blackwell unit; this
+// file holds the single-CTA kernel and what both kernels share (the CTA-pair
+// kernel is in gemm_kernel_pair.cuh):
 //
-//   * one CTA per SM loops over output tiles of BM x BN = 128 x 256 in a
-//     banded order (the pages' grid swizzle, generalised to ragged grids);
-//   * warp 4 (one thread) streams A and B boxes with TMA into a 4-stage ring
-//     of 128-byte-swizzled shared-memory tiles (the hardware swizzle replaces
-//     the pages' hand-derived XOR layouts); for an operand whose rows TMA
-//     cannot address (row pitch not a multiple of 16 bytes) warps 6-9 copy it
-//     with cp.async into the same swizzled image;
-//   * warp 5 (one thread) issues tcgen05.mma 128 x 256 x (32 bytes of K) with
-//     the accumulator in tensor memory, two accumulators of 256 columns so the
-//     epilogue of one tile overlaps the k-loop of the next;
+//   * one CTA per SM loops over output tiles of BM x BN = 128 x (256, 224,
+//     192 or 128) in a banded order (the pages' grid swizzle, generalised to
+//     ragged grids and to strided batches of products);
+//   * warp 4 streams A and B boxes with TMA (3-D tensor maps: the batch's
+//     matrix is the outer coordinate) into a ring of 128-byte-swizzled
+//     shared-memory stages (the hardware swizzle replaces the pages'
+//     hand-derived XOR layouts); for an operand whose rows TMA cannot address
+//     (row pitch not a multiple of 16 bytes) and that was not packed, warps
+//     6-9 copy it with cp.async into the same swizzled image;
+//   * warp 5 issues tcgen05.mma 128 x BN x (32 bytes of K) -- kind::f16,
+//     kind::tf32 or kind::f8f6f4 -- into one of two accumulators in tensor
+//     memory, so the epilogue of one tile overlaps the k-loop of the next;
 //   * warps 0-3 read the accumulator with tcgen05.ld (warp w owns TMEM lanes
-//     32w..32w+31 = tile rows), convert and store C.
+//     32w..32w+31 = tile rows), apply the optional fused epilogue, convert,
+//     stage 32 x 64-byte pieces in shared memory and store them with TMA.
 //
 // Every wait on an mbarrier is bounded: past the launch's time limit the
 // waiting thread records a timeout in the device status word and the CTA
