@@ -21,6 +21,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdgt_gemm.so")
+# The checked build: every range check in the kernels compiled in (DGT_CHECKED=1).
+LIB_CHECKED = os.path.join(PKG, "libdgt_gemm_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -44,23 +46,28 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile and link the library; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, checked: bool = False) -> str:
+    """Compile and link the library (``checked``: the range-checked debug
+    build, ``libdgt_gemm_checked.so``); returns its path."""
+    lib = LIB_CHECKED if checked else LIB
+    if not force and up_to_date(lib):
+        return lib
+    bdir = os.path.join(BUILD, "checked") if checked else BUILD
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if checked:
+        extra += ["-DDGT_CHECKED=1"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(bdir, os.path.basename(src).replace(".cu", ".o"))
         cmd = [cc, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -71,14 +78,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="-v" in sys.argv,
+                checked="--checked" in sys.argv))

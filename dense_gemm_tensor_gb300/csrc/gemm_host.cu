@@ -615,6 +615,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     p.num_work = p.tail_start + rest * plan.segs;
     p.ws_ctr = reinterpret_cast<unsigned long long*>(ws);
     p.ws = reinterpret_cast<float*>(ws + kCounterBytes);
+    p.ws_slots = static_cast<long long>(rest) * plan.segs * 2 * plan.pairs;
   }
   if (pack_a && ws != nullptr) {
     if (launch_pack(A, lda * es, ws + off_a, lda_p * es, M, K * es, ga, stream, dev->sm_count) != cudaSuccess)

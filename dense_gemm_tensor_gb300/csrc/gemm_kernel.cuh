@@ -37,6 +37,15 @@
 
 #include "ptx.cuh"
 
+// A checked build (-DDGT_CHECKED=1) tests, before each shared-memory, tensor
+// memory, TMA-coordinate and scratch access the kernels compute, that it lies
+// in its range; a failing access is skipped and recorded in the device status
+// word (kind 3, the site in bits 4-11), where compute-sanitizer cannot run.
+// The default build compiles every check away.
+#ifndef DGT_CHECKED
+#define DGT_CHECKED 0
+#endif
+
 // Geometry of the 32-byte-atom swizzle (MN-major 32-bit operands): stride
 // between K-row groups in the descriptor, and which row bits select the
 // XOR pattern of the 32-byte chunks.
@@ -109,6 +118,7 @@ __device__ __forceinline__ void mma_issue_pair(uint32_t d, uint64_t a, uint64_t 
 // Status word codes (device status[0]); status[1] holds the epoch of the last aborted launch.
 enum : uint32_t {
   STATUS_TIMEOUT = 1u,
+  STATUS_OUT_OF_RANGE = 3u,  // a checked build skipped an access outside its range
   ROLE_PRODUCER = 1u << 4,
   ROLE_MMA = 2u << 4,
   ROLE_EPILOGUE = 3u << 4,
@@ -158,6 +168,24 @@ struct GemmParams {
   int act;
   float alpha, beta;
   const void* bias;
+  long long ws_slots;  // fp32 partial tiles the split-tail scratch holds (range checks of a checked build)
+};
+
+// Arrival counters of split tiles the scratch holds: one per CTA of a cluster
+// of up to four, for up to 1024 split work tiles.
+constexpr int kSplitCounters = 1024 * 4;
+
+// Sites of the checked build's range checks (status bits 4-11).
+enum : uint32_t {
+  CHECK_A_STAGE = 1u,     // TMA destination of an A box inside its stage
+  CHECK_B_STAGE = 2u,     // TMA destination of a B box inside its stage
+  CHECK_TMA_X = 3u,       // innermost TMA coordinate on a 16-byte boundary
+  CHECK_ACC_COLS = 4u,    // accumulator columns inside the allocated tensor memory
+  CHECK_DESC = 5u,        // MMA operand descriptors inside the stage
+  CHECK_STAGING = 6u,     // epilogue staging tile inside the warp's ring
+  CHECK_TMEM_LD = 7u,     // tensor-memory columns the epilogue reads
+  CHECK_SPLIT_SLOT = 8u,  // fp32 partial tile inside the scratch
+  CHECK_SPLIT_CTR = 9u,   // arrival counter inside the scratch
 };
 
 // Output staging in shared memory (see epi_chunk_addr): each epilogue warp
@@ -176,6 +204,7 @@ struct EpiRing {
   uint32_t base;  // this warp's first tile
   int bufs;
   int next;
+  uint32_t end;   // end of the staging area (range checks of a checked build)
 };
 
 template <int KIND, bool B_KMAJOR, int BN_>
@@ -237,6 +266,22 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb,
   const int r = t - g * band;
   mb = first_m + r % rows;
   nb = r / rows;
+}
+
+static __device__ __noinline__ void record_out_of_range(const GemmParams& p, uint32_t site) {
+  atomicCAS(p.status, 0u, STATUS_OUT_OF_RANGE | ((site & 0xFFu) << 4) | ((blockIdx.x & 0xFFFFu) << 16));
+  atomicExch(p.status + 1, p.epoch);  // the launch winds down like one that timed out
+  __threadfence();
+}
+
+// true when the access may go ahead; in a checked build a false `ok` is recorded.
+__device__ __forceinline__ bool in_range(const GemmParams& p, bool ok, uint32_t site) {
+  if constexpr (DGT_CHECKED != 0) {
+    if (!ok) record_out_of_range(p, site);
+    return ok;
+  } else {
+    return true;
+  }
 }
 
 static __device__ __noinline__ void record_timeout(const GemmParams& p, uint32_t code) {
@@ -397,8 +442,9 @@ __device__ __forceinline__ uint32_t epi_chunk_addr(uint32_t stage, int r, int j)
 // read it (only lane 0 has stores in flight; up to bufs - 1 younger ones may
 // still be reading their tiles).
 __device__ __forceinline__ uint32_t epi_acquire(const GemmParams& p, int lane, EpiRing& ring) {
-  const uint32_t stage = ring.base + static_cast<uint32_t>(ring.next % ring.bufs) * EPI_WARP_BYTES;
+  uint32_t stage = ring.base + static_cast<uint32_t>(ring.next % ring.bufs) * EPI_WARP_BYTES;
   ++ring.next;
+  if (!in_range(p, stage >= ring.base && stage + EPI_WARP_BYTES <= ring.end, CHECK_STAGING)) stage = ring.base;
   if (p.c_tma && lane == 0) {
     switch (ring.bufs) {
       case 1: bulk_wait_read<0>(); break;
@@ -702,16 +748,19 @@ __global__ void __launch_bounds__(320, 1)
           }
           const uint32_t fb = full0 + 8 * s;
           mbar_arrive_expect_tx(fb, tx);
-          if (p.a_tma) tma_load_3d(sA + s * Cf::A_BYTES, &tmA, fb, kb * Cf::BK, mb * Cf::BM, za);
-          if (p.b_tma) {
+          const bool kx = in_range(p, (kb * Cf::BK * Cf::ES) % 16 == 0, CHECK_TMA_X);
+          if (p.a_tma && kx && in_range(p, s < S && sA + (s + 1) * Cf::A_BYTES <= sB, CHECK_A_STAGE))
+            tma_load_3d(sA + s * Cf::A_BYTES, &tmA, fb, kb * Cf::BK, mb * Cf::BM, za);
+          if (p.b_tma && in_range(p, s < S && sB + (s + 1) * Cf::B_BYTES <= sE, CHECK_B_STAGE)) {
             if constexpr (B_KMAJOR) {
-              tma_load_3d(sB + s * Cf::B_BYTES, &tmB, fb, kb * Cf::BK, nb * Cf::BN, zb);
+              if (kx) tma_load_3d(sB + s * Cf::B_BYTES, &tmB, fb, kb * Cf::BK, nb * Cf::BN, zb);
             } else {
 #pragma unroll
               for (int j = 0; j < Cf::NBOX; ++j)
-                tma_load_3d(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES,
-                            (j == Cf::NBOX - 1 && Cf::LASTN != Cf::BOXN) ? &tmB2 : &tmB, fb,
-                            nb * Cf::BN + j * Cf::BOXN, kb * Cf::BK, zb);
+                if (in_range(p, ((nb * Cf::BN + j * Cf::BOXN) * Cf::ES) % 16 == 0, CHECK_TMA_X))
+                  tma_load_3d(sB + s * Cf::B_BYTES + j * Cf::BOX_BYTES,
+                              (j == Cf::NBOX - 1 && Cf::LASTN != Cf::BOXN) ? &tmB2 : &tmB, fb,
+                              nb * Cf::BN + j * Cf::BOXN, kb * Cf::BK, zb);
             }
           }
         }
@@ -740,8 +789,11 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
           const uint32_t a_addr = sA + s * Cf::A_BYTES;
           const uint32_t b_addr = sB + s * Cf::B_BYTES;
+          const bool mma_ok =
+              in_range(p, a_addr + Cf::A_BYTES <= sB && b_addr + Cf::B_BYTES <= sE, CHECK_DESC) &&
+              in_range(p, (d & 0xFFFFu) - (tmem & 0xFFFFu) + Cf::BN <= uint32_t(Cf::TMEM_COLS), CHECK_ACC_COLS);
 #pragma unroll
-          for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
+          for (int kk = 0; kk < Cf::KSTEPS && mma_ok; ++kk) {
             const uint64_t ad = sdesc(a_addr + kk * 32, 16, 1024, SWZ_128B);
             uint64_t bd;
             if constexpr (B_KMAJOR)
@@ -764,7 +816,8 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue
     int tc = 0;
-    EpiRing ring{sE + static_cast<uint32_t>(warp * Cf::EPI_BUFS * EPI_WARP_BYTES), Cf::EPI_BUFS, 0};
+    EpiRing ring{sE + static_cast<uint32_t>(warp * Cf::EPI_BUFS * EPI_WARP_BYTES), Cf::EPI_BUFS, 0,
+                 sE + static_cast<uint32_t>(Cf::EPI_BUFS * EPI_BYTES)};
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tc) {
       int mb, nb, bz;
       tile_coords(p, t, mb, nb, bz);
@@ -774,7 +827,8 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const int row0 = mb * Cf::BM + warp * 32;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
-      const int ncols = min(Cf::BN, p.N - nb * Cf::BN);
+      int ncols = min(Cf::BN, p.N - nb * Cf::BN);
+      if (!in_range(p, b * Cf::ACC_COLS + ((ncols + 31) / 32) * 32 <= Cf::TMEM_COLS, CHECK_TMEM_LD)) ncols = 0;
       for_each_acc_chunk(taddr, (ncols + 31) / 32, [&](int c, const uint32_t(&r)[32]) {
         emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, nb * Cf::BN + c * 32, bz, r);
       });

@@ -219,7 +219,10 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t fb = mapa_shared(full0 + 8 * s, lead);
           const uint32_t a_dst = sA + s * Cf::A_BYTES;
           const uint32_t b_dst = sB + s * Cf::B_BYTES;
-          if (elect_one()) {
+          const bool ld_ok = in_range(p, s < S && a_dst + Cf::A_BYTES <= sB, CHECK_A_STAGE) &&
+                             in_range(p, b_dst + Cf::B_BYTES <= sE, CHECK_B_STAGE) &&
+                             in_range(p, (kb * Cf::BK * Cf::ES) % 16 == 0 && (col0 * Cf::ES) % 16 == 0, CHECK_TMA_X);
+          if (ld_ok && elect_one()) {
             if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_TX);
             if constexpr (PAIRS == 1) {
               tma_load_3d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0, za);
@@ -268,6 +271,9 @@ __global__ void __launch_bounds__(192, 1)
           tc_fence_after();
           const uint32_t a_addr = sA + s * Cf::A_BYTES;
           const uint32_t b_addr = sB + s * Cf::B_BYTES;
+          const bool mma_ok =
+              in_range(p, a_addr + Cf::A_BYTES <= sB && b_addr + Cf::B_BYTES <= sE, CHECK_DESC) &&
+              in_range(p, (d & 0xFFFFu) - (tmem & 0xFFFFu) + BN <= uint32_t(Cf::TMEM_COLS), CHECK_ACC_COLS);
           uint64_t ad[Cf::KSTEPS], bd[Cf::KSTEPS];
 #pragma unroll
           for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
@@ -278,7 +284,7 @@ __global__ void __launch_bounds__(192, 1)
               bd[kk] = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
           }
           const uint32_t first = (kb == wk.kb0) ? 0u : 1u;
-          if (elect_one()) {
+          if (mma_ok && elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
               const uint32_t acc = kk > 0 ? 1u : first;
@@ -305,7 +311,8 @@ __global__ void __launch_bounds__(192, 1)
     // barrier publishes the outcome), so the barriers below always see all 128.
     const int tid = threadIdx.x;  // 0..127
     int tc = 0;
-    EpiRing ring{sE + static_cast<uint32_t>(warp * Cf::EPI_BUFS * EPI_WARP_BYTES), Cf::EPI_BUFS, 0};
+    EpiRing ring{sE + static_cast<uint32_t>(warp * Cf::EPI_BUFS * EPI_WARP_BYTES), Cf::EPI_BUFS, 0,
+                 sE + static_cast<uint32_t>(Cf::EPI_BUFS * EPI_BYTES)};
     for (int w = pair; w < p.num_work; w += npairs, ++tc) {
       const PairWork wk = pair_work(p, w);
       const int b = tc % NB;
@@ -318,13 +325,19 @@ __global__ void __launch_bounds__(192, 1)
       const int row0 = wk.mb * Cf::BMP + int(half) * Cf::BM + warp * 32;  // first of this warp's 32 rows
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
       const int ncols = min(BN, p.N - nbt * BN);
-      const int nchunks = ncols > 0 ? (ncols + 31) / 32 : 0;
+      int nchunks = ncols > 0 ? (ncols + 31) / 32 : 0;
+      if (!in_range(p, b * Cf::ACC_COLS + nchunks * 32 <= Cf::TMEM_COLS, CHECK_TMEM_LD)) nchunks = 0;
       const int col0 = nbt * BN;
       if (wk.f < 0) {
         for_each_acc_chunk(taddr, nchunks,
                            [&](int c, const uint32_t(&r)[32]) { emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, r); });
       } else {
         // split tile: publish this segment's partial, then find out whether it is the last
+        // (every slot this tile's segments use, and its counters, lie in the scratch)
+        const bool slots_ok =
+            in_range(p, static_cast<long long>(wk.f + 1) * p.tail_segs * CL <= p.ws_slots, CHECK_SPLIT_SLOT) &&
+            in_range(p, (wk.f + 1) * CL <= kSplitCounters, CHECK_SPLIT_CTR);
+        if (!slots_ok) nchunks = 0;
         float4* mine = reinterpret_cast<float4*>(
             p.ws + (static_cast<long long>(wk.f * p.tail_segs + wk.seg) * CL + rank) * Cf::PARTIAL_FLOATS);
         for_each_acc_chunk(taddr, nchunks, [&](int c, const uint32_t(&r)[32]) {
@@ -337,7 +350,7 @@ __global__ void __launch_bounds__(192, 1)
         __threadfence();
         epilogue_barrier();
         if (tid == 0) {
-          const int arrival = arrive_split(p, p.ws_ctr + wk.f * CL + rank);
+          const int arrival = slots_ok ? arrive_split(p, p.ws_ctr + wk.f * CL + rank) : 0;
           *last_slot = (arrival + 1 == p.tail_segs) ? 1 : 0;
         }
         epilogue_barrier();

@@ -54,7 +54,7 @@ cudaError_t launch_pack(const void* src, int64_t src_ld_bytes, void* dst, int64_
 
 // Split-tail scratch layout: arrival counters (one per CTA of a cluster of up
 // to four) for up to 1024 split work tiles, then the fp32 partial tiles.
-constexpr size_t kSplitCounterBytes = 1024 * 4 * sizeof(unsigned long long);
+constexpr size_t kSplitCounterBytes = kSplitCounters * sizeof(unsigned long long);
 
 // Caller-owned scratch for the split tail (instead of the per-stream buffer
 // the library allocates): device address and capacity in bytes.
