@@ -147,6 +147,16 @@ _FN = {}  # dtype -> bound C function, filled on first use
 _FN_EX = {}
 
 
+def _raw_stream(stream, device_index: int) -> int:
+    """The cudaStream_t of `stream`, or of the device's current stream."""
+    if stream is not None:
+        return stream.cuda_stream
+    try:  # the current stream's handle without building a Stream object
+        return torch._C._cuda_getCurrentRawStream(device_index)
+    except AttributeError:
+        return torch.cuda.current_stream(device_index).cuda_stream
+
+
 def _rows(t: torch.Tensor, what: str) -> int:
     """Leading dimension of a 2-D tensor with unit column stride."""
     if t.dim() != 2:
@@ -200,7 +210,7 @@ def matmul(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *,
         out = torch.empty((M, N), dtype=dt, device=A.device)
     elif out.dtype != dt or tuple(out.shape) != (M, N):
         raise ValueError("out must be M x N with the operands' dtype")
-    s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    s = _raw_stream(stream, torch.cuda.current_device())
     if alpha == 1.0 and beta == 0.0 and bias is None and activation is None:
         code = fn(M, N, K, A.data_ptr() or None, _rows(A, "A"), B.data_ptr() or None, _rows(B, "B"),
                   out.data_ptr() or None, _rows(out, "out"), layout, s)
@@ -250,7 +260,7 @@ def _matmul_fp8(A, B, out, layout, stream, alpha, beta, bias, activation):
                              not bias.is_cuda or (N > 1 and bias.stride(0) != 1)):
         raise ValueError("bias must be a contiguous CUDA bfloat16 vector of N elements")
     epi = Epilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None, ACTIVATIONS[activation])
-    s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    s = _raw_stream(stream, torch.cuda.current_device())
     fn = getattr(load(), _FP8[dt])
     code = fn(M, N, K, A.data_ptr() or None, _rows(A, "A"), B.data_ptr() or None, _rows(B, "B"),
               out.data_ptr() or None, _rows(out, "out"), layout, ctypes.byref(epi), s)
@@ -288,7 +298,7 @@ def bmm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, la
                              (N > 1 and bias.stride(0) != 1)):
         raise ValueError("bias must be a contiguous CUDA vector of N elements of the operands' dtype")
     epi = Epilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None, ACTIVATIONS[activation])
-    s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    s = _raw_stream(stream, torch.cuda.current_device())
     ld = lambda t: t.stride(1) if t.shape[1] > 1 else t.shape[2]  # noqa: E731
     bs = lambda t: t.stride(0) if t.shape[0] > 1 else 0  # noqa: E731
     name = _BY_DTYPE[dt] + "_strided_batched"
