@@ -433,110 +433,140 @@ struct Batch {
   int64_t count = 1, stride_a = 0, stride_b = 0, stride_c = 0;
 };
 
-int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
-             void* C, int64_t ldc, int layout, void* stream_ptr, const ExternalScratch* ext = nullptr,
-             const gemm_epilogue_t* epi = nullptr, const Batch& bat = Batch()) {
-  const bool fp8 = kind == KIND_E4M3 || kind == KIND_E5M2;
-  const int es = (kind == KIND_TF32) ? 4 : fp8 ? 1 : 2;  // operand element size
-  const int eo = (kind == KIND_TF32) ? 4 : 2;             // output element size (FP8 writes bfloat16)
-  const int out_kind = fp8 ? int(KIND_BF16) : kind;
+// One call of the C interface, with the quantities derived from its kind.
+struct Call {
+  int kind;
+  bool fp8;
+  int es;        // operand element size in bytes
+  int eo;        // output element size (FP8 writes bfloat16)
+  int out_kind;  // kind whose output type C has
+  int64_t M, N, K;
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  void* C;
+  int64_t ldc;
+  int layout;
+  Batch bat;
+  const gemm_epilogue_t* epi;
+  bool fused;        // the epilogue is not the identity
+  const void* bias;  // fused ? epi->bias : nullptr
+  cudaStream_t stream;
+  const ExternalScratch* ext;
+};
+
+// Argument rules of the C interface that need no device (sizes, leading
+// dimensions, batch strides, epilogue code, element alignment).
+int check_arguments(const Call& c) {
   const int64_t kLim = (int64_t(1) << 31) - 1;
+  const int64_t M = c.M, N = c.N, K = c.K;
   if (M < 0 || N < 0 || K < 0 || M > kLim || N > kLim || K > kLim) return GEMM_ERR_INVALID_VALUE;
-  if (layout != GEMM_B_ROW_MAJOR && layout != GEMM_B_K_MAJOR) return GEMM_ERR_INVALID_VALUE;
-  const int64_t nbat = bat.count;
-  if (nbat < 0 || bat.stride_a < 0 || bat.stride_b < 0 || bat.stride_c < 0) return GEMM_ERR_INVALID_VALUE;
-  if (M == 0 || N == 0 || nbat == 0) return GEMM_OK;
-  if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_VALUE;
-  if (nbat > 1) {
+  if (c.layout != GEMM_B_ROW_MAJOR && c.layout != GEMM_B_K_MAJOR) return GEMM_ERR_INVALID_VALUE;
+  const Batch& bat = c.bat;
+  if (bat.count < 0 || bat.stride_a < 0 || bat.stride_b < 0 || bat.stride_c < 0) return GEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0 || bat.count == 0) return GEMM_OK;
+  if (c.C == nullptr || c.ldc < N) return GEMM_ERR_INVALID_VALUE;
+  if (bat.count > 1) {
     // the C matrices must not overlap one another; A and B may repeat (stride 0) but not overlap partly
-    if (bat.stride_c < (M - 1) * ldc + N) return GEMM_ERR_INVALID_VALUE;
-    if (K > 0 && bat.stride_a != 0 && bat.stride_a < (M - 1) * lda + K) return GEMM_ERR_INVALID_VALUE;
-    const int64_t b_ext = layout == GEMM_B_ROW_MAJOR ? (K - 1) * ldb + N : (N - 1) * ldb + K;
+    if (bat.stride_c < (M - 1) * c.ldc + N) return GEMM_ERR_INVALID_VALUE;
+    if (K > 0 && bat.stride_a != 0 && bat.stride_a < (M - 1) * c.lda + K) return GEMM_ERR_INVALID_VALUE;
+    const int64_t b_ext = c.layout == GEMM_B_ROW_MAJOR ? (K - 1) * c.ldb + N : (N - 1) * c.ldb + K;
     if (K > 0 && bat.stride_b != 0 && bat.stride_b < b_ext) return GEMM_ERR_INVALID_VALUE;
     if (bat.stride_a > (int64_t(1) << 40) || bat.stride_b > (int64_t(1) << 40) || bat.stride_c > (int64_t(1) << 40))
       return GEMM_ERR_INVALID_VALUE;
-    if (nbat > kLim) return GEMM_ERR_INVALID_VALUE;
+    if (bat.count > kLim) return GEMM_ERR_INVALID_VALUE;
   }
   if (K > 0) {
-    if (A == nullptr || B == nullptr || lda < K) return GEMM_ERR_INVALID_VALUE;
-    if (ldb < (layout == GEMM_B_ROW_MAJOR ? N : K)) return GEMM_ERR_INVALID_VALUE;
-    if (lda > (int64_t(1) << 40) / es || ldb > (int64_t(1) << 40) / es) return GEMM_ERR_INVALID_VALUE;
+    if (c.A == nullptr || c.B == nullptr || c.lda < K) return GEMM_ERR_INVALID_VALUE;
+    if (c.ldb < (c.layout == GEMM_B_ROW_MAJOR ? N : K)) return GEMM_ERR_INVALID_VALUE;
+    if (c.lda > (int64_t(1) << 40) / c.es || c.ldb > (int64_t(1) << 40) / c.es) return GEMM_ERR_INVALID_VALUE;
   }
-  if (ldc > (int64_t(1) << 40) / eo) return GEMM_ERR_INVALID_VALUE;
-  if (((M + 127) / 128) * ((N + 127) / 128) > kLim / nbat) return GEMM_ERR_INVALID_VALUE;
-
-  if (epi != nullptr && (epi->activation < GEMM_ACT_NONE || epi->activation > GEMM_ACT_GELU_TANH))
+  if (c.ldc > (int64_t(1) << 40) / c.eo) return GEMM_ERR_INVALID_VALUE;
+  if (((M + 127) / 128) * ((N + 127) / 128) > kLim / bat.count) return GEMM_ERR_INVALID_VALUE;
+  if (c.epi != nullptr && (c.epi->activation < GEMM_ACT_NONE || c.epi->activation > GEMM_ACT_GELU_TANH))
     return GEMM_ERR_INVALID_VALUE;
-  // the fused epilogue is on unless it is the identity
-  const bool fused = epi != nullptr && !(epi->alpha == 1.0f && epi->beta == 0.0f && epi->bias == nullptr &&
-                                         epi->activation == GEMM_ACT_NONE);
-  const void* bias = fused ? epi->bias : nullptr;
   auto mis = [](const void* p, int size) { return (reinterpret_cast<uintptr_t>(p) % size) != 0; };
-  if (mis(C, eo) || (K > 0 && (mis(A, es) || mis(B, es))) || (bias != nullptr && mis(bias, eo)))
+  if (mis(c.C, c.eo) || (K > 0 && (mis(c.A, c.es) || mis(c.B, c.es))) || (c.bias != nullptr && mis(c.bias, c.eo)))
     return GEMM_ERR_MISALIGNED;
+  return GEMM_OK;
+}
 
-  const DeviceInfo* dev = nullptr;
-  int st = current_device(&dev);
-  if (st != GEMM_OK) return st;
-
+// Memory rules that need the device: every pointer is device memory, and C
+// overlaps neither an operand of the batch nor the bias.
+int check_memory(const Call& c) {
+  const int64_t nbat = c.bat.count;
   uintptr_t c0, c1;
-  extent(C, M, N, ldc, eo, &c0, &c1);
-  c1 += static_cast<uintptr_t>((nbat - 1) * bat.stride_c * eo);  // every matrix of the batch
-  if (!is_device_memory(C)) return GEMM_ERR_NOT_DEVICE_MEMORY;
-  if (bias != nullptr) {
-    const uintptr_t s0 = reinterpret_cast<uintptr_t>(bias), s1 = s0 + uintptr_t(N) * eo;
+  extent(c.C, c.M, c.N, c.ldc, c.eo, &c0, &c1);
+  c1 += static_cast<uintptr_t>((nbat - 1) * c.bat.stride_c * c.eo);  // every matrix of the batch
+  if (!is_device_memory(c.C)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+  if (c.bias != nullptr) {
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(c.bias), s1 = s0 + uintptr_t(c.N) * c.eo;
     if (overlaps(c0, c1, s0, s1)) return GEMM_ERR_INVALID_VALUE;
-    if (!is_device_memory(bias)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+    if (!is_device_memory(c.bias)) return GEMM_ERR_NOT_DEVICE_MEMORY;
   }
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-
-  if (K == 0) {
-    for (int64_t z = 0; z < nbat; ++z) {
-      void* Cz = static_cast<char*>(C) + z * bat.stride_c * eo;
-      cudaError_t e;
-      if (fused) {
-        GemmParams ep;
-        memset(&ep, 0, sizeof(ep));
-        ep.alpha = epi->alpha;
-        ep.beta = epi->beta;
-        ep.bias = bias;
-        ep.act = epi->activation;
-        e = launch_epilogue_only(out_kind, Cz, ldc, int(M), int(N), ep, stream, dev->sm_count);
-      } else {
-        e = launch_fill_zero(Cz, ldc, int(M), int(N), eo, stream, dev->sm_count);
-      }
-      if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
-      g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
-    return GEMM_OK;
-  }
-
+  if (c.K == 0) return GEMM_OK;
   uintptr_t a0, a1, b0, b1;
-  extent(A, M, K, lda, es, &a0, &a1);
-  if (layout == GEMM_B_ROW_MAJOR)
-    extent(B, K, N, ldb, es, &b0, &b1);
+  extent(c.A, c.M, c.K, c.lda, c.es, &a0, &a1);
+  if (c.layout == GEMM_B_ROW_MAJOR)
+    extent(c.B, c.K, c.N, c.ldb, c.es, &b0, &b1);
   else
-    extent(B, N, K, ldb, es, &b0, &b1);
-  a1 += static_cast<uintptr_t>((nbat - 1) * bat.stride_a * es);
-  b1 += static_cast<uintptr_t>((nbat - 1) * bat.stride_b * es);
+    extent(c.B, c.N, c.K, c.ldb, c.es, &b0, &b1);
+  a1 += static_cast<uintptr_t>((nbat - 1) * c.bat.stride_a * c.es);
+  b1 += static_cast<uintptr_t>((nbat - 1) * c.bat.stride_b * c.es);
   if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return GEMM_ERR_INVALID_VALUE;
-  if (!is_device_memory(A) || !is_device_memory(B)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+  if (!is_device_memory(c.A) || !is_device_memory(c.B)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+  return GEMM_OK;
+}
 
-  LaunchPlan L;
-  memset(&L, 0, sizeof(L));
-  GemmParams& p = L.p;
-  int ga = granularity(A, lda, es), gb = granularity(B, ldb, es);
+// K = 0: C = 0, or act(beta C + bias) with a fused epilogue, matrix by matrix.
+int run_k_zero(const Call& c, const DeviceInfo* dev) {
+  for (int64_t z = 0; z < c.bat.count; ++z) {
+    void* Cz = static_cast<char*>(c.C) + z * c.bat.stride_c * c.eo;
+    cudaError_t e;
+    if (c.fused) {
+      GemmParams ep;
+      memset(&ep, 0, sizeof(ep));
+      ep.alpha = c.epi->alpha;
+      ep.beta = c.epi->beta;
+      ep.bias = c.bias;
+      ep.act = c.epi->activation;
+      e = launch_epilogue_only(c.out_kind, Cz, c.ldc, int(c.M), int(c.N), ep, c.stream, dev->sm_count);
+    } else {
+      e = launch_fill_zero(Cz, c.ldc, int(c.M), int(c.N), c.eo, c.stream, dev->sm_count);
+    }
+    if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return GEMM_OK;
+}
+
+// Operands as the kernel reads them, after any packing or transposition.
+struct Operands {
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  int ga, gb;   // row granularity (16: TMA-addressable)
+  bool kmajor;  // B K-major as read by the kernel
+};
+
+// Chooses the plan, sets up the stream's scratch ([counters][split partials]
+// [packed A][packed B]), launches the packing / transposition copies, and
+// fills the work-decomposition fields of p. Returns a status.
+int prepare(const Call& c, const DeviceInfo* dev, int dev_id, TilePlan& plan, Operands& op, GemmParams& p) {
+  const int es = c.es;
+  const int64_t M = c.M, N = c.N, K = c.K, nbat = c.bat.count;
+  op = Operands{c.A, c.lda, c.B, c.ldb, granularity(c.A, c.lda, es), granularity(c.B, c.ldb, es), false};
   if (nbat > 1) {
     // a batch is streamed by TMA in place: rows and matrix strides on 16-byte boundaries
-    if (ga < 16 || gb < 16 || (bat.stride_a * es) % 16 != 0 || (bat.stride_b * es) % 16 != 0 || fp8)
+    if (op.ga < 16 || op.gb < 16 || (c.bat.stride_a * es) % 16 != 0 || (c.bat.stride_b * es) % 16 != 0 || c.fp8)
       return GEMM_ERR_MISALIGNED;
   }
   // The FP8 kernels read B K-major only: a row-major FP8 B is transposed into
   // the stream's scratch first (the packed-B slot), and from then on it is K-major.
-  const bool transpose_b = fp8 && layout == GEMM_B_ROW_MAJOR;
-  const bool kmajor = layout == GEMM_B_K_MAJOR || transpose_b;
-  int dev_id = 0;
-  cudaGetDevice(&dev_id);
+  const bool transpose_b = c.fp8 && c.layout == GEMM_B_ROW_MAJOR;
+  op.kmajor = c.layout == GEMM_B_K_MAJOR || transpose_b;
   // Operands whose rows TMA cannot address (row starts not 16-byte aligned)
   // are packed into 128-byte-aligned rows in the stream's scratch first (a
   // bandwidth-bound copy), so that the TMA kernels run; without scratch the
@@ -547,20 +577,19 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   // copy pays for itself once the other output dimension is a few thousand.
   // FP8 operands always go through TMA (the copy warps do not handle 1-byte
   // granules), so they are packed whenever they need it.
-  const bool may_pack = nbat == 1 && ext == nullptr &&
-                        (fp8 || !(g_debug_flags.load(std::memory_order_relaxed) & DEBUG_NO_PACK));
+  const bool may_pack = nbat == 1 && c.ext == nullptr &&
+                        (c.fp8 || !(g_debug_flags.load(std::memory_order_relaxed) & DEBUG_NO_PACK));
   auto off_line = [es](const void* ptr, int64_t ld) {
     return ((reinterpret_cast<uintptr_t>(ptr) | static_cast<uintptr_t>(ld * es)) % 128) != 0;
   };
   const bool big = 2.0 * double(M) * double(N) * double(K) >= 1.6e10;
-  const bool pack_a = may_pack && (ga < 16 || (big && N >= 2048 && off_line(A, lda)));
-  const bool pack_b = may_pack && (transpose_b || gb < 16 || (big && M >= 2048 && off_line(B, ldb)));
-  TilePlan plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, (ga == 16 || pack_a) && (gb == 16 || pack_b),
-                              dev->sm_count, nbat);
-  // Scratch for this plan, laid out as [counters][split partials][packed A][packed B].
-  const int64_t lda_p = pack_a ? (K * es + 127) / 128 * 128 / es : lda;
-  const int64_t b_rows = kmajor ? N : K, b_cols = kmajor ? K : N;  // of the operand the kernel reads
-  const int64_t ldb_p = pack_b ? (b_cols * es + 127) / 128 * 128 / es : ldb;
+  const bool pack_a = may_pack && (op.ga < 16 || (big && N >= 2048 && off_line(c.A, c.lda)));
+  const bool pack_b = may_pack && (transpose_b || op.gb < 16 || (big && M >= 2048 && off_line(c.B, c.ldb)));
+  plan = choose_plan(dev_id, c.kind, M, N, K, es, op.kmajor, (op.ga == 16 || pack_a) && (op.gb == 16 || pack_b),
+                     dev->sm_count, nbat);
+  const int64_t lda_p = pack_a ? (K * es + 127) / 128 * 128 / es : c.lda;
+  const int64_t b_rows = op.kmajor ? N : K, b_cols = op.kmajor ? K : N;  // of the operand the kernel reads
+  const int64_t ldb_p = pack_b ? (b_cols * es + 127) / 128 * 128 / es : c.ldb;
   auto split_tiles = [&](const TilePlan& pl) {
     const int64_t tm = (M + (pl.pair ? 255 : 127)) / (pl.pair ? 256 : 128);
     const int64_t tn = ((N + pl.bn - 1) / pl.bn + pl.pairs - 1) / pl.pairs;
@@ -568,31 +597,31 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     return (r > 0 && r <= 1024) ? int(r) : 0;
   };
   int rest = split_tiles(plan);
-  size_t split_bytes = rest ? workspace_bytes(rest, plan.segs, plan.bn, 2 * plan.pairs) : 0;
+  const size_t split_bytes = rest ? workspace_bytes(rest, plan.segs, plan.bn, 2 * plan.pairs) : 0;
   const size_t off_a = (split_bytes + 255) / 256 * 256;
   const size_t off_b = off_a + (pack_a ? (size_t(M) * size_t(lda_p) * es + 255) / 256 * 256 : 0);
   const size_t total = off_b + (pack_b ? size_t(b_rows) * size_t(ldb_p) * es : 0);
   char* ws = nullptr;
-  if (ext != nullptr) {
+  if (c.ext != nullptr) {
     if (rest) {
-      if (split_bytes > ext->bytes) return GEMM_ERR_SCRATCH_LIMIT;
-      ws = static_cast<char*>(ext->ptr);
+      if (split_bytes > c.ext->bytes) return GEMM_ERR_SCRATCH_LIMIT;
+      ws = static_cast<char*>(c.ext->ptr);
     }
   } else if (total > 0) {
-    ws = static_cast<char*>(stream_workspace(dev_id, stream, total < kCounterBytes ? kCounterBytes : total));
+    ws = static_cast<char*>(stream_workspace(dev_id, c.stream, total < kCounterBytes ? kCounterBytes : total));
     if (ws == nullptr) {
       // no scratch: no split tail, and unaligned operands are read in place by the copy warps
-      if (fp8 && (pack_a || pack_b)) return GEMM_ERR_LAUNCH;  // FP8 cannot do without the packed copy
+      if (c.fp8 && (pack_a || pack_b)) return GEMM_ERR_LAUNCH;  // FP8 cannot do without the packed copy
       if (pack_a || pack_b)
-        plan = choose_plan(dev_id, kind, M, N, K, es, kmajor, ga == 16 && gb == 16, dev->sm_count, nbat);
+        plan = choose_plan(dev_id, c.kind, M, N, K, es, op.kmajor, op.ga == 16 && op.gb == 16, dev->sm_count, nbat);
       rest = 0;
     }
   }
-  const int bn = plan.bn;
+  // work decomposition: tiles along N count pairs of adjacent tiles for the
+  // shared-A kernel (the second past the last column when the count is odd:
+  // computed, not stored)
   const int64_t tiles_m = (M + (plan.pair ? 255 : 127)) / (plan.pair ? 256 : 128);
-  // work tiles along N: the shared-A kernel takes two adjacent tiles at a time
-  // (the second past the last column when the count is odd: computed, not stored)
-  const int64_t tiles_n = ((N + bn - 1) / bn + plan.pairs - 1) / plan.pairs;
+  const int64_t tiles_n = ((N + plan.bn - 1) / plan.bn + plan.pairs - 1) / plan.pairs;
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
@@ -601,9 +630,9 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   p.batch = int(nbat);
   p.tiles_per_batch = int(tiles_m * tiles_n);
   p.num_tiles = int(nbat * tiles_m * tiles_n);
-  p.stride_a = nbat > 1 ? bat.stride_a : 0;
-  p.stride_b = nbat > 1 ? bat.stride_b : 0;
-  p.stride_c = nbat > 1 ? bat.stride_c : 0;
+  p.stride_a = nbat > 1 ? c.bat.stride_a : 0;
+  p.stride_b = nbat > 1 ? c.bat.stride_b : 0;
+  p.stride_c = nbat > 1 ? c.bat.stride_c : 0;
   p.num_kb = int((K * es + 127) / 128);
   p.raster = plan.raster;
   p.tail_start = p.num_tiles;
@@ -618,113 +647,170 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     p.ws_slots = static_cast<long long>(rest) * plan.segs * 2 * plan.pairs;
   }
   if (pack_a && ws != nullptr) {
-    if (launch_pack(A, lda * es, ws + off_a, lda_p * es, M, K * es, ga, stream, dev->sm_count) != cudaSuccess)
+    if (launch_pack(c.A, c.lda * es, ws + off_a, lda_p * es, M, K * es, op.ga, c.stream, dev->sm_count) !=
+        cudaSuccess)
       return GEMM_ERR_LAUNCH;
-    A = ws + off_a;
-    lda = lda_p;
-    ga = 16;
+    op.A = ws + off_a;
+    op.lda = lda_p;
+    op.ga = 16;
   }
   if (pack_b && ws != nullptr) {
     if (transpose_b) {
-      if (launch_transpose_bytes(B, ldb, ws + off_b, ldb_p, K, N, stream, dev->sm_count) != cudaSuccess)
+      if (launch_transpose_bytes(c.B, c.ldb, ws + off_b, ldb_p, K, N, c.stream, dev->sm_count) != cudaSuccess)
         return GEMM_ERR_LAUNCH;
-    } else if (launch_pack(B, ldb * es, ws + off_b, ldb_p * es, b_rows, b_cols * es, gb, stream, dev->sm_count) !=
-               cudaSuccess) {
+    } else if (launch_pack(c.B, c.ldb * es, ws + off_b, ldb_p * es, b_rows, b_cols * es, op.gb, c.stream,
+                           dev->sm_count) != cudaSuccess) {
       return GEMM_ERR_LAUNCH;
     }
-    B = ws + off_b;
-    ldb = ldb_p;
-    gb = 16;
+    op.B = ws + off_b;
+    op.ldb = ldb_p;
+    op.gb = 16;
   }
-  if (plan.pair && !(ga == 16 && gb == 16)) return GEMM_ERR_LAUNCH;  // the pair kernel needs TMA operands
-  p.A = A;
-  p.lda = lda;
-  p.B = B;
-  p.ldb = ldb;
+  if (plan.pair && !(op.ga == 16 && op.gb == 16)) return GEMM_ERR_LAUNCH;  // the pair kernel needs TMA operands
+  return GEMM_OK;
+}
+
+// The tensor maps of A, B (and the last, narrower B box) and C.
+int encode_maps(const Call& c, const TilePlan& plan, const Operands& op, LaunchPlan& L) {
+  const GemmParams& p = L.p;
+  const int es = c.es, eo = c.eo, bn = plan.bn;
+  const uint64_t nbat = uint64_t(c.bat.count);
+  const CUtensorMapDataType dt = c.kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : c.kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : c.kind == KIND_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType dt_out = c.fp8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : dt;
+  const uint32_t bk = 128 / es;  // K elements per 128-byte row
+  const uint64_t za = p.stride_a ? nbat : 1, zb = p.stride_b ? nbat : 1;
+  const uint64_t M = uint64_t(c.M), N = uint64_t(c.N), K = uint64_t(c.K);
+  // A box: 128 rows, or 64 where two pairs each load half a CTA's rows for both
+  if (p.a_tma && !encode_3d(&L.tmA, dt, op.A, K, M, uint64_t(op.lda) * es, za, uint64_t(p.stride_a) * es, bk,
+                            (plan.pair && plan.pairs == 2) ? 64 : 128))
+    return GEMM_ERR_DRIVER;
+  if (p.b_tma) {
+    bool ok;
+    if (op.kmajor) {
+      ok = encode_3d(&L.tmB, dt, op.B, K, N, uint64_t(op.ldb) * es, zb, uint64_t(p.stride_b) * es, bk,
+                     uint32_t(plan.pair ? bn / 2 : bn));
+    } else {
+      const CUtensorMapSwizzle swz = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+      ok = encode_3d(&L.tmB, dt, op.B, N, K, uint64_t(op.ldb) * es, zb, uint64_t(p.stride_b) * es, 128 / es, bk, swz);
+      // the last box of a tile whose columns per CTA are not whole 128-byte boxes
+      const int cols = plan.pair ? bn / 2 : bn, boxn = 128 / es;
+      const int lastn = cols - (cols + boxn - 1) / boxn * boxn + boxn;
+      if (ok && lastn != boxn)
+        ok = encode_3d(&L.tmB2, dt, op.B, N, K, uint64_t(op.ldb) * es, zb, uint64_t(p.stride_b) * es,
+                       uint32_t(lastn), bk, swz);
+    }
+    if (!ok) return GEMM_ERR_DRIVER;
+  }
+  // C box: 32 rows x 64 bytes, the staging tile of one epilogue warp (64-byte swizzle)
+  if (p.c_tma && !encode_3d(&L.tmC, dt_out, c.C, N, M, uint64_t(c.ldc) * eo, p.stride_c ? nbat : 1,
+                            uint64_t(p.stride_c) * eo, uint32_t(64 / eo), 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return GEMM_ERR_DRIVER;
+  return GEMM_OK;
+}
+
+int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+             void* C, int64_t ldc, int layout, void* stream_ptr, const ExternalScratch* ext = nullptr,
+             const gemm_epilogue_t* epi = nullptr, const Batch& bat = Batch()) {
+  Call c;
+  c.kind = kind;
+  c.fp8 = kind == KIND_E4M3 || kind == KIND_E5M2;
+  c.es = (kind == KIND_TF32) ? 4 : c.fp8 ? 1 : 2;
+  c.eo = (kind == KIND_TF32) ? 4 : 2;
+  c.out_kind = c.fp8 ? int(KIND_BF16) : kind;
+  c.M = M;
+  c.N = N;
+  c.K = K;
+  c.A = A;
+  c.lda = lda;
+  c.B = B;
+  c.ldb = ldb;
+  c.C = C;
+  c.ldc = ldc;
+  c.layout = layout;
+  c.bat = bat;
+  c.epi = epi;
+  c.fused = epi != nullptr && !(epi->alpha == 1.0f && epi->beta == 0.0f && epi->bias == nullptr &&
+                                epi->activation == GEMM_ACT_NONE);
+  c.bias = c.fused ? epi->bias : nullptr;
+  c.stream = static_cast<cudaStream_t>(stream_ptr);
+  c.ext = ext;
+
+  int st = check_arguments(c);
+  if (st != GEMM_OK || M == 0 || N == 0 || bat.count == 0) return st;
+  const DeviceInfo* dev = nullptr;
+  st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  st = check_memory(c);
+  if (st != GEMM_OK) return st;
+  if (K == 0) return run_k_zero(c, dev);
+
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  LaunchPlan L;
+  memset(&L, 0, sizeof(L));
+  GemmParams& p = L.p;
+  TilePlan plan;
+  Operands op;
+  st = prepare(c, dev, dev_id, plan, op, p);
+  if (st != GEMM_OK) return st;
+  p.A = op.A;
+  p.lda = op.lda;
+  p.B = op.B;
+  p.ldb = op.ldb;
   p.C = C;
   p.ldc = ldc;
-  p.a_tma = ga == 16;
-  p.b_tma = gb == 16;
+  p.a_tma = op.ga == 16;
+  p.b_tma = op.gb == 16;
   p.copy_bytes = 16;
-  if (!p.a_tma) p.copy_bytes = ga;
-  if (!p.b_tma && gb < p.copy_bytes) p.copy_bytes = gb;
-  p.c_gran = granularity(C, ldc, eo);
-  p.c_tma = p.c_gran == 16;
+  if (!p.a_tma) p.copy_bytes = op.ga;
+  if (!p.b_tma && op.gb < p.copy_bytes) p.copy_bytes = op.gb;
+  p.c_gran = granularity(C, ldc, c.eo);
+  // TMA stores of C need 16-byte rows, base and (in a batch) matrix stride; else row stores
+  p.c_tma = p.c_gran == 16 && (p.stride_c * c.eo) % 16 == 0;
   p.status = dev->status_words;
   uint32_t ep = g_epoch.fetch_add(1, std::memory_order_relaxed);
   if (ep == 0) ep = g_epoch.fetch_add(1, std::memory_order_relaxed);
   p.epoch = ep;
   p.debug = g_debug_flags.load(std::memory_order_relaxed);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-  p.fused = fused ? 1 : 0;
-  if (fused) {
+  p.fused = c.fused ? 1 : 0;
+  if (c.fused) {
     p.alpha = epi->alpha;
     p.beta = epi->beta;
-    p.bias = bias;
+    p.bias = c.bias;
     p.act = epi->activation;
   }
-
-  const CUtensorMapDataType dt = kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                 : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                 : kind == KIND_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  const CUtensorMapDataType dt_out = fp8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : dt;
-  const uint32_t bk = 128 / es;  // K elements per 128-byte row
-  // A box: 128 rows, or 64 where two pairs each load half a CTA's rows for both
-  const uint64_t za = p.stride_a ? uint64_t(nbat) : 1, zb = p.stride_b ? uint64_t(nbat) : 1;
-  if (p.a_tma && !encode_3d(&L.tmA, dt, A, uint64_t(K), uint64_t(M), uint64_t(lda) * es, za,
-                            uint64_t(p.stride_a) * es, bk, (plan.pair && plan.pairs == 2) ? 64 : 128))
-    return GEMM_ERR_DRIVER;
-  if (p.b_tma) {
-    bool ok;
-    if (kmajor) {
-      ok = encode_3d(&L.tmB, dt, B, uint64_t(K), uint64_t(N), uint64_t(ldb) * es, zb, uint64_t(p.stride_b) * es, bk,
-                     uint32_t(plan.pair ? bn / 2 : bn));
-    } else {
-      const CUtensorMapSwizzle swz = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
-      ok = encode_3d(&L.tmB, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, zb, uint64_t(p.stride_b) * es,
-                     128 / es, bk, swz);
-      // the last box of a tile whose columns per CTA are not whole 128-byte boxes
-      const int cols = plan.pair ? bn / 2 : bn, boxn = 128 / es;
-      const int lastn = cols - (cols + boxn - 1) / boxn * boxn + boxn;
-      if (ok && lastn != boxn)
-        ok = encode_3d(&L.tmB2, dt, B, uint64_t(N), uint64_t(K), uint64_t(ldb) * es, zb, uint64_t(p.stride_b) * es,
-                       uint32_t(lastn), bk, swz);
-    }
-    if (!ok) return GEMM_ERR_DRIVER;
-  }
-  // C box: 32 rows x 64 bytes, the staging tile of one epilogue warp (64-byte swizzle)
-  if (p.c_tma && (p.stride_c * eo) % 16 != 0) p.c_tma = 0;  // matrices of C off 16-byte boundaries: row stores
-  if (p.c_tma && !encode_3d(&L.tmC, dt_out, C, uint64_t(N), uint64_t(M), uint64_t(ldc) * eo,
-                            p.stride_c ? uint64_t(nbat) : 1, uint64_t(p.stride_c) * eo, uint32_t(64 / eo), 32,
-                            CU_TENSOR_MAP_SWIZZLE_64B))
-    return GEMM_ERR_DRIVER;
-  L.b_kmajor = kmajor;
+  st = encode_maps(c, plan, op, L);
+  if (st != GEMM_OK) return st;
+  L.b_kmajor = op.kmajor;
   L.pair = plan.pair;
   L.pairs = plan.pairs;
-  L.bn = bn;
+  L.bn = plan.bn;
   L.grid = plan.grid;
   L.threads = (p.a_tma && p.b_tma) ? 192 : 320;
-  L.stream = stream;
+  L.stream = c.stream;
 
   // internal consistency of the derived launch parameters (a violation is a library bug)
   if (p.raster < 1 || p.num_kb < 1 || p.num_tiles < 1 || p.num_work < p.num_tiles || p.tail_segs < 1 ||
       p.tail_segs > kMaxTailSegs || L.grid < 1 || (L.pair && (L.grid % (2 * L.pairs) != 0)) || p.tiles_n < 1 ||
       p.tiles_m < 1 || (L.pair && L.pairs != 1 && L.pairs != 2) || (!L.pair && L.pairs != 1))
     return GEMM_ERR_LAUNCH;
-  if (fp8 && !(p.a_tma && p.b_tma && kmajor)) return GEMM_ERR_LAUNCH;  // guaranteed by the packing above
+  if (c.fp8 && !(p.a_tma && p.b_tma && op.kmajor)) return GEMM_ERR_LAUNCH;  // guaranteed by prepare()
   cudaError_t e;
   switch (kind) {
-    case KIND_TF32: e = kmajor ? launch_tf32_km(L) : launch_tf32_rm(L); break;
-    case KIND_BF16: e = kmajor ? launch_bf16_km(L) : launch_bf16_rm(L); break;
-    case KIND_F16: e = kmajor ? launch_f16_km(L) : launch_f16_rm(L); break;
+    case KIND_TF32: e = op.kmajor ? launch_tf32_km(L) : launch_tf32_rm(L); break;
+    case KIND_BF16: e = op.kmajor ? launch_bf16_km(L) : launch_bf16_rm(L); break;
+    case KIND_F16: e = op.kmajor ? launch_f16_km(L) : launch_f16_rm(L); break;
     case KIND_E4M3: e = launch_e4m3_km(L); break;
     default: e = launch_e5m2_km(L); break;
   }
   if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  const int32_t info[8] = {plan.pair ? 2 * plan.pairs : 1, bn, p.raster, L.grid, p.tail_segs, plan.conc, p.tail_start,
-                           p.num_work};
+  const int32_t info[8] = {plan.pair ? 2 * plan.pairs : 1, plan.bn, p.raster, L.grid, p.tail_segs, plan.conc,
+                           p.tail_start, p.num_work};
   memcpy(t_last_plan, info, sizeof(info));
   return GEMM_OK;
 }
