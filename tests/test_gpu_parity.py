@@ -308,3 +308,19 @@ def test_matmul_from_host_pipelined(dtype, layout, chunks):
     for _ in range(2):  # the second call reuses the cached buffers and streams
         C = gemm.matmul_from_host(p.a.pin_memory(), p.b.pin_memory(), layout=layout, buffers=bufs, chunks=chunks)
     _check_full(p, C)
+
+
+@pytest.mark.parametrize("dtype,shape", [
+    ("bf16", (256, 200, 1 << 18)),     # 2048 k-slabs: long accumulation, split segments of hundreds of slabs
+    ("tf32", (130, 260, 1 << 16)),
+    ("bf16", (1 << 20, 8, 64)),        # tall and skinny: 4096 tile rows
+    ("f16", (8, 1 << 20, 64)),         # short and wide: thousands of tile columns, one ragged row block
+])
+def test_extreme_aspect_and_long_k(dtype, shape):
+    """Long K (fp32 accumulation over 2^16-2^18 products) and extreme aspect
+    ratios (one dimension 2^20, the others tiny), checked on sampled entries
+    including every corner and the last row and column."""
+    M, N, K = shape
+    p = inputs.make_problem("extreme", dtype, M, N, K, seed_a=M % 97 + 1, seed_b=N % 89 + 2, dist_a="normal")
+    C, _ = _run(p)
+    _check_sampled(p, C, seed=M + N + K, count=2048)
