@@ -2,7 +2,6 @@
 oracle (oracle/batched.py): every matrix of the batch in full, with the
 single product's acceptance rule (oracle/check.py)."""
 
-import numpy as np
 import pytest
 import torch
 

@@ -7,7 +7,6 @@ so the error budget is that of the FP16/BF16 products), with the fused
 epilogue's scale where one is applied.
 """
 
-import numpy as np
 import pytest
 import torch
 
