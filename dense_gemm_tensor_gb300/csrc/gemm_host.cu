@@ -476,6 +476,8 @@ int check_arguments(const Call& c) {
     if (bat.stride_a > (int64_t(1) << 40) || bat.stride_b > (int64_t(1) << 40) || bat.stride_c > (int64_t(1) << 40))
       return GEMM_ERR_INVALID_VALUE;
     if (bat.count > kLim) return GEMM_ERR_INVALID_VALUE;
+    // FP8 B is read K-major; a batch is not transposed
+    if (c.fp8 && c.layout != GEMM_B_K_MAJOR) return GEMM_ERR_INVALID_VALUE;
   }
   if (K > 0) {
     if (c.A == nullptr || c.B == nullptr || c.lda < K) return GEMM_ERR_INVALID_VALUE;
@@ -560,7 +562,7 @@ int prepare(const Call& c, const DeviceInfo* dev, int dev_id, TilePlan& plan, Op
   op = Operands{c.A, c.lda, c.B, c.ldb, granularity(c.A, c.lda, es), granularity(c.B, c.ldb, es), false};
   if (nbat > 1) {
     // a batch is streamed by TMA in place: rows and matrix strides on 16-byte boundaries
-    if (op.ga < 16 || op.gb < 16 || (c.bat.stride_a * es) % 16 != 0 || (c.bat.stride_b * es) % 16 != 0 || c.fp8)
+    if (op.ga < 16 || op.gb < 16 || (c.bat.stride_a * es) % 16 != 0 || (c.bat.stride_b * es) % 16 != 0)
       return GEMM_ERR_MISALIGNED;
   }
   // The FP8 kernels read B K-major only: a row-major FP8 B is transposed into
@@ -914,6 +916,22 @@ int gemm_bf16_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, co
                               void* stream) {
   const dgt::Batch b{batch, stride_a, stride_b, stride_c};
   return dgt::run_gemm(dgt::KIND_BF16, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue, b);
+}
+
+int gemm_e4m3_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                              int64_t stride_a, const uint8_t* B, int64_t ldb, int64_t stride_b, uint16_t* C,
+                              int64_t ldc, int64_t stride_c, int layout, const gemm_epilogue_t* epilogue,
+                              void* stream) {
+  const dgt::Batch b{batch, stride_a, stride_b, stride_c};
+  return dgt::run_gemm(dgt::KIND_E4M3, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue, b);
+}
+
+int gemm_e5m2_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                              int64_t stride_a, const uint8_t* B, int64_t ldb, int64_t stride_b, uint16_t* C,
+                              int64_t ldc, int64_t stride_c, int layout, const gemm_epilogue_t* epilogue,
+                              void* stream) {
+  const dgt::Batch b{batch, stride_a, stride_b, stride_c};
+  return dgt::run_gemm(dgt::KIND_E5M2, M, N, K, A, lda, B, ldb, C, ldc, layout, stream, nullptr, epilogue, b);
 }
 
 int gemm_e4m3(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,

@@ -49,7 +49,7 @@ EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_tf32_ex", "gemm_f16_ex", 
            "gemm_status_string", "gemm_get_device_status", "gemm_reset_device_status", "gemm_set_debug",
            "gemm_launch_count", "gemm_set_tuning", "gemm_last_plan", "gemm_free_workspaces",
            "gemm_bf16_static_scratch", "gemm_tf32_strided_batched", "gemm_f16_strided_batched",
-           "gemm_bf16_strided_batched")
+           "gemm_bf16_strided_batched", "gemm_e4m3_strided_batched", "gemm_e5m2_strided_batched")
 
 _lib = None
 
@@ -78,7 +78,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, ctypes.POINTER(Epilogue), vp]
         fn.restype = ctypes.c_int
-    for name in ("gemm_tf32_strided_batched", "gemm_f16_strided_batched", "gemm_bf16_strided_batched"):
+    for name in ("gemm_tf32_strided_batched", "gemm_f16_strided_batched", "gemm_bf16_strided_batched",
+                 "gemm_e4m3_strided_batched", "gemm_e5m2_strided_batched"):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64, ctypes.c_int,
                        ctypes.POINTER(Epilogue), vp]
@@ -275,10 +276,13 @@ def bmm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, la
     """Strided batch C[z] = A[z] . B[z] (gemm_*_strided_batched), optionally
     with the fused epilogue. A: batch x M x K; B: batch x K x N (layout 0) or
     batch x N x K (layout 1); a batch stride of 0 (``expand``) repeats one
-    matrix. Rows must be contiguous; the other strides come from the tensors."""
+    matrix. Rows must be contiguous; the other strides come from the tensors.
+    FP8 operands (float8_e4m3fn, float8_e5m2) need a K-major B and give a
+    bfloat16 C."""
     dt = A.dtype
-    if dt not in _BY_DTYPE or B.dtype != dt:
-        raise TypeError("A and B must both be float32, float16 or bfloat16")
+    if (dt not in _BY_DTYPE and dt not in _FP8) or B.dtype != dt:
+        raise TypeError("A and B must both be float32, float16, bfloat16, float8_e4m3fn or float8_e5m2")
+    out_dt = torch.bfloat16 if dt in _FP8 else dt
     if A.dim() != 3 or B.dim() != 3 or A.shape[0] != B.shape[0]:
         raise ValueError("A and B must be 3-D with the same batch size")
     batch, M, K = A.shape
@@ -286,22 +290,22 @@ def bmm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, la
     if (B.shape[1] if layout == GEMM_B_ROW_MAJOR else B.shape[2]) != K:
         raise ValueError("B's K dimension does not match A")
     if out is None:
-        out = torch.empty((batch, M, N), dtype=dt, device=A.device)
-    elif out.dtype != dt or tuple(out.shape) != (batch, M, N):
-        raise ValueError("out must be batch x M x N with the operands' dtype")
+        out = torch.empty((batch, M, N), dtype=out_dt, device=A.device)
+    elif out.dtype != out_dt or tuple(out.shape) != (batch, M, N):
+        raise ValueError("out must be batch x M x N of the output dtype")
     for t, what in ((A, "A"), (B, "B"), (out, "out")):
         if t.shape[2] > 1 and t.stride(2) != 1:
             raise ValueError(f"{what} must have unit stride along its rows")
     if activation not in ACTIVATIONS:
         raise ValueError(f"activation must be one of {sorted(k for k in ACTIVATIONS if k)}")
-    if bias is not None and (bias.dtype != dt or bias.dim() != 1 or bias.numel() != N or not bias.is_cuda or
+    if bias is not None and (bias.dtype != out_dt or bias.dim() != 1 or bias.numel() != N or not bias.is_cuda or
                              (N > 1 and bias.stride(0) != 1)):
-        raise ValueError("bias must be a contiguous CUDA vector of N elements of the operands' dtype")
+        raise ValueError("bias must be a contiguous CUDA vector of N elements of the output dtype")
     epi = Epilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None, ACTIVATIONS[activation])
     s = _raw_stream(stream, torch.cuda.current_device())
     ld = lambda t: t.stride(1) if t.shape[1] > 1 else t.shape[2]  # noqa: E731
     bs = lambda t: t.stride(0) if t.shape[0] > 1 else 0  # noqa: E731
-    name = _BY_DTYPE[dt] + "_strided_batched"
+    name = (_FP8[dt] if dt in _FP8 else _BY_DTYPE[dt]) + "_strided_batched"
     code = getattr(load(), name)(batch, M, N, K, A.data_ptr() or None, ld(A), bs(A), B.data_ptr() or None, ld(B),
                                  bs(B), out.data_ptr() or None, ld(out), bs(out) if batch > 1 else 0, layout,
                                  ctypes.byref(epi), s)

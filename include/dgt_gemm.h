@@ -190,6 +190,21 @@ int gemm_e5m2(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, co
               uint16_t* C, int64_t ldc, int layout, const gemm_epilogue_t* epilogue, void* stream);
 
 /*
+ * Strided batches of FP8 products (the rules of the strided-batch calls
+ * above): B must be K-major (layout 1; GEMM_ERR_INVALID_VALUE otherwise), and
+ * for batch > 1 the rows and matrix strides of A and B must be 16-byte
+ * multiples (GEMM_ERR_MISALIGNED otherwise); nothing is packed or transposed.
+ */
+int gemm_e4m3_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                              int64_t stride_a, const uint8_t* B, int64_t ldb, int64_t stride_b, uint16_t* C,
+                              int64_t ldc, int64_t stride_c, int layout, const gemm_epilogue_t* epilogue,
+                              void* stream);
+int gemm_e5m2_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                              int64_t stride_a, const uint8_t* B, int64_t ldb, int64_t stride_b, uint16_t* C,
+                              int64_t ldc, int64_t stride_c, int layout, const gemm_epilogue_t* epilogue,
+                              void* stream);
+
+/*
  * gemm_bf16_static_scratch: gemm_bf16 for callers that cannot allocate.
  * (The GEMM pages have no counterpart to this call.)
  *

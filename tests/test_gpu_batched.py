@@ -10,7 +10,8 @@ from dense_gemm_tensor_gb300 import gemm, inputs
 
 pytestmark = pytest.mark.gpu
 
-TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "tf32": torch.float32}
+TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "tf32": torch.float32, "e4m3": torch.float8_e4m3fn,
+            "e5m2": torch.float8_e5m2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,7 +31,7 @@ def _lib():
 def _batch(dtype, batch, rows, cols, seed, gap_rows=0, dist="uniform"):
     """batch x rows x cols operand whose matrices sit gap_rows padded rows
     apart (NaN in the gaps); returns (tensor view, flat CPU buffer, ld, stride)."""
-    pad = 8 if dtype != "tf32" else 4
+    pad = 16 // TORCH_DT[dtype].itemsize  # 16-byte rows
     ld = -(-cols // pad) * pad
     stride = (rows + gap_rows) * ld
     buf = torch.full((batch * stride,), float("nan"), dtype=TORCH_DT[dtype])
@@ -157,3 +158,23 @@ def test_batched_argument_errors():
     # negative batch; batch 0 is a no-op
     assert fn(-1, 64, 64, 64, pa, 64, 4096, pa, 64, 4096, pc, 64, 4096, 0, None, None) == gemm.GEMM_ERR_INVALID_VALUE
     assert fn(0, 64, 64, 64, pa, 64, 4096, pa, 64, 4096, pc, 64, 4096, 0, None, None) == gemm.GEMM_OK
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_batched_fp8(fmt):
+    """FP8 batches (K-major B, bfloat16 C), with a shared B and with one per matrix."""
+    batch, M, N, K = 4, 300, 272, 384
+    A, a_buf, lda, sa = _batch(fmt, batch, M, K, 1100, dist="normal")
+    B, b_buf, ldb, sb = _batch(fmt, batch, N, K, 1200, dist="normal")
+    av, bv = oracle.decode_fp8(a_buf, fmt), oracle.decode_fp8(b_buf, fmt)
+    C = gemm.bmm(_dev(a_buf, A), _dev(b_buf, B), layout=1)
+    torch.cuda.synchronize()
+    _check_batch("bf16", C, batch, M, N, K, av, lda, sa, bv, ldb, sb, 1)
+    B1 = _dev(b_buf, B)[:1].expand(batch, N, K)
+    C = gemm.bmm(_dev(a_buf, A), B1, layout=1)
+    torch.cuda.synchronize()
+    _check_batch("bf16", C, batch, M, N, K, av, lda, sa, bv, ldb, 0, 1)
+    # a row-major FP8 B is not taken in a batch
+    fn = gemm.load().gemm_e4m3_strided_batched
+    pa, pc = _dev(a_buf, A).data_ptr(), C.data_ptr()
+    assert fn(2, 64, 64, 64, pa, 64, 4096, pa, 64, 4096, pc, 64, 4096, 0, None, None) == gemm.GEMM_ERR_INVALID_VALUE
