@@ -324,3 +324,19 @@ def test_extreme_aspect_and_long_k(dtype, shape):
     p = inputs.make_problem("extreme", dtype, M, N, K, seed_a=M % 97 + 1, seed_b=N % 89 + 2, dist_a="normal")
     C, _ = _run(p)
     _check_sampled(p, C, seed=M + N + K, count=2048)
+
+
+def test_fp16_overflow_is_ieee_infinity():
+    """Products beyond the binary16 range round to +-inf (RNE overflow); the
+    last representable magnitude 65504 stays finite."""
+    M, N, K = 4, 8, 16
+    A = torch.full((M, K), 16.0, dtype=torch.float16, device="cuda")
+    B = torch.full((K, N), 16.0, dtype=torch.float16, device="cuda")   # each entry 16*16*16 = 4096
+    B[:, 1] = 300.0                                                     # 16*300*16 = 76800 > 65504
+    B[:, 2] = -300.0
+    B[:, 3] = 255.875                                                   # 16*255.875*16 = 65504
+    C = gemm.matmul(A, B)
+    torch.cuda.synchronize()
+    assert torch.all(C[:, 0] == 4096.0)
+    assert torch.all(C[:, 1] == float("inf")) and torch.all(C[:, 2] == float("-inf"))
+    assert torch.all(C[:, 3] == 65504.0)
