@@ -126,6 +126,14 @@ __device__ __forceinline__ int arrive_split(const GemmParams& p, unsigned long l
   return 0;
 }
 
+// k-slab taken at step i of a work item in the pair's round `round`. Rounds
+// alternate direction, so each round starts on the slabs that the previous
+// round (whose tiles ran in step with this one's) read last, while they are
+// still in L2.
+__device__ __forceinline__ int pair_kb(const PairWork& wk, int i, int round) {
+  return (round & 1) ? wk.kb1 - 1 - i : wk.kb0 + i;
+}
+
 __device__ __forceinline__ void epilogue_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <int KIND, bool B_KMAJOR, int BN, int PAIRS>
@@ -202,14 +210,15 @@ __global__ void __launch_bounds__(192, 1)
     // The whole warp walks the loop (so addresses and coordinates stay
     // warp-uniform); one elected lane issues.
     if (!(p.debug & DEBUG_STALL_PRODUCER)) {
-      int it = 0;
+      int it = 0, tc = 0;
       bool ok = true;
-      for (int w = pair; ok && w < p.num_work; w += npairs) {
+      for (int w = pair; ok && w < p.num_work; w += npairs, ++tc) {
         const PairWork wk = pair_work(p, w);
         const int row0 = wk.mb * Cf::BMP + int(half) * Cf::BM;
         const int col0 = (wk.nb * PAIRS + q) * BN + int(half) * Cf::BNH;
         const int za = p.stride_a ? wk.bz : 0, zb = p.stride_b ? wk.bz : 0;  // a stride of 0 repeats matrix 0
-        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
+        for (int i = 0; i < wk.kb1 - wk.kb0; ++i, ++it) {
+          const int kb = pair_kb(wk, i, tc);
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!warp_wait_phase(p, empty0 + 8 * s, ph ^ 1, ROLE_PRODUCER | (s << 8))) {
@@ -261,7 +270,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!warp_wait_phase(p, acce0 + 8 * b, use ^ 1, ROLE_MMA | (0x80u << 8))) break;
         tc_fence_after();
         const uint32_t d = tmem + b * Cf::ACC_COLS;
-        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
+        for (int i = 0; i < wk.kb1 - wk.kb0; ++i, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!warp_wait_phase(p, full0 + 8 * s, ph, ROLE_MMA | (s << 8))) {
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(192, 1)
             else
               bd[kk] = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
           }
-          const uint32_t first = (kb == wk.kb0) ? 0u : 1u;
+          const uint32_t first = (i == 0) ? 0u : 1u;  // the accumulator restarts at a work item's first step
           if (mma_ok && elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
