@@ -55,8 +55,14 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def peak_for(dtype: str, peaks: dict) -> float:
-    return peaks["bf16_tflops"] * NOMINAL_RATIO[dtype]
+def peak_for(dtype: str, peaks: dict, sustained: bool = True) -> float:
+    """Dense tensor peak for ``dtype`` in TFLOP/s: the measured BF16 figure times
+    the nominal ratio. The sustained figure (a seconds-long loop under the power
+    cap) is the one for kernels timed inside the long back-to-back loop here;
+    the burst figure is for a kernel timed alone."""
+    burst = peaks["bf16_tflops"]
+    base = peaks.get("bf16_tflops_sustained", burst) if sustained else burst
+    return base * NOMINAL_RATIO[dtype]
 
 
 def reduce_max(value: float, world: int, device=None) -> float:
@@ -201,9 +207,9 @@ def run_ours(args, world, rank, local):
         ms = statistics.mean(e[dt][0].elapsed_time(e[dt][1]) for e in evs)
         ach = FLOP_PER_PRODUCT / (ms * 1e-3) / 1e12
         pk = peak_for(dt, peaks)
-        pk_sus = peaks.get("bf16_tflops_sustained", pk) * NOMINAL_RATIO[dt]
+        pk_burst = peak_for(dt, peaks, sustained=False)
         per_dtype[dt] = {"kernel_ms": round(ms, 5), "tflops": round(ach, 2), "peak_tflops": round(pk, 1),
-                         "frac": round(ach / pk, 4), "frac_of_sustained_peak": round(ach / pk_sus, 4)}
+                         "frac": round(ach / pk, 4), "frac_of_burst_peak": round(ach / pk_burst, 4)}
     dominant = max(DTYPES, key=lambda d: per_dtype[d]["kernel_ms"])
     total_flop = FLOP_PER_PRODUCT * len(DTYPES) * args.steps * world
     value = total_flop / (elapsed_ms * 1e-3) / 1e12
@@ -250,8 +256,10 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "tensor", "kernel": kernel_name(dominant, plans[dominant]),
                      "plan": {k: plans[dominant][k] for k in ("kernel", "tile_n", "raster", "tail_segs")},
                      "achieved": per_dtype[dominant]["tflops"], "peak": per_dtype[dominant]["peak_tflops"],
-                     "unit": "TFLOP/s", "frac": per_dtype[dominant]["frac"], "traffic": None,
-                     "peak_source": f"{peak_src} bf16 burst x nominal {dominant}/bf16 ratio"},
+                     "unit": "TFLOP/s", "frac": per_dtype[dominant]["frac"],
+                     "frac_of_burst_peak": per_dtype[dominant]["frac_of_burst_peak"], "traffic": None,
+                     "peak_source": f"{peak_src} bf16 sustained (timed inside a long power-capped loop) "
+                                    f"x nominal {dominant}/bf16 ratio"},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "clocks": clocks.summary(),
