@@ -314,23 +314,47 @@ def bmm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, la
     return out
 
 
+_COPY_STREAMS: dict = {}
+
+
+def _copy_streams(dev: torch.device) -> tuple:
+    """One host-to-device and one device-to-host stream per device, shared by
+    every end-to-end call, so the copies of consecutive calls queue in call
+    order instead of competing for the host link."""
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    if idx not in _COPY_STREAMS:
+        _COPY_STREAMS[idx] = (torch.cuda.Stream(idx), torch.cuda.Stream(idx))
+    return _COPY_STREAMS[idx]
+
+
 def matmul_from_host(A_host: torch.Tensor, B_host: torch.Tensor, *, layout: int = GEMM_B_ROW_MAJOR,
                      device: torch.device | str = "cuda", stream: torch.cuda.Stream | None = None,
-                     buffers: dict | None = None, chunks: int | None = None) -> torch.Tensor:
+                     buffers: dict | None = None, chunks: int | None = None, wait: bool = True):
     """End-to-end product of host operands: copy A and B to the device, run
-    the kernels, copy C back into a pinned host tensor, and synchronise.
+    the kernels, copy C back into a pinned host tensor.
 
     B is copied first; A is then streamed in row blocks: block i's product
     runs while block i+1 is copied in and block i-1's rows of C are copied out
-    (three streams, ordered by events), so the host<->device copies in both
+    (a copy-in and a copy-out stream shared by all calls on the device, and the
+    compute stream, ordered by events), so the host<->device copies in both
     directions overlap each other and the kernels. ``chunks`` sets the number
     of row blocks (default: one per 1024 rows of A, at most 4). ``buffers``
-    (optional, reused across calls) caches the device and pinned host buffers,
-    streams and events so repeated calls do not allocate.
+    (optional, reused across calls) caches the device and pinned host buffers
+    so repeated calls do not allocate.
+
+    With ``wait`` (the default) the call synchronises and returns C. With
+    ``wait=False`` it returns ``(C, event)`` at once: C is valid once ``event``
+    has completed, and the copies of a following call queue behind this one's,
+    so several products can be in flight. A call that reuses ``buffers`` first
+    waits (on the host) for the previous call on them to finish, since it
+    overwrites their contents, C among them. ``A_host`` and ``B_host`` must
+    stay unchanged until the call's event has completed.
     """
     buffers = {} if buffers is None else buffers
     dev = torch.device(device)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    if buffers.get("done") is not None:
+        buffers["done"].synchronize()
     M = A_host.shape[0]
     N = B_host.shape[1] if layout == GEMM_B_ROW_MAJOR else B_host.shape[0]
     out_dtype = torch.bfloat16 if A_host.dtype in _FP8 else A_host.dtype
@@ -340,13 +364,12 @@ def matmul_from_host(A_host: torch.Tensor, B_host: torch.Tensor, *, layout: int 
                        a=torch.empty(A_host.shape, dtype=A_host.dtype, device=dev),
                        b=torch.empty(B_host.shape, dtype=B_host.dtype, device=dev),
                        c=torch.empty((M, N), dtype=out_dtype, device=dev),
-                       c_host=torch.empty((M, N), dtype=out_dtype, pin_memory=True),
-                       s_in=torch.cuda.Stream(dev), s_out=torch.cuda.Stream(dev))
+                       c_host=torch.empty((M, N), dtype=out_dtype, pin_memory=True))
     n = chunks if chunks is not None else max(1, min(4, M // 1024))
     n = max(1, min(n, M)) if M > 0 else 1
     bounds = [M * i // n for i in range(n + 1)]
     a, b, c, c_host = buffers["a"], buffers["b"], buffers["c"], buffers["c_host"]
-    s_in, s_out = buffers["s_in"], buffers["s_out"]
+    s_in, s_out = _copy_streams(dev)
     start = torch.cuda.Event()
     start.record(s)
     s_in.wait_event(start)
@@ -368,9 +391,13 @@ def matmul_from_host(A_host: torch.Tensor, B_host: torch.Tensor, *, layout: int 
         s_out.wait_event(computed)
         with torch.cuda.stream(s_out):
             c_host[lo:hi].copy_(c[lo:hi], non_blocking=True)
-    s_out.synchronize()
-    s.synchronize()
-    return c_host
+    done = torch.cuda.Event()
+    done.record(s_out)  # after the last kernel (s_out waited for it) and the last copy out
+    buffers["done"] = done
+    if wait:
+        done.synchronize()
+        return c_host
+    return c_host, done
 
 
 def device_status(stream: torch.cuda.Stream | None = None) -> int:

@@ -310,6 +310,30 @@ def test_matmul_from_host_pipelined(dtype, layout, chunks):
     _check_full(p, C)
 
 
+def test_matmul_from_host_many_in_flight():
+    """Three end-to-end products enqueued at once (wait=False): their copies
+    queue on the device's shared copy streams while earlier products compute;
+    every entry of each result checked. A call that reuses a pending call's
+    buffers waits for it, and returns its own product."""
+    probs = [inputs.make_problem("fly", "tf32", 1500, 900, 700, seed_a=81, seed_b=82),
+             inputs.make_problem("fly", "f16", 2100, 640, 1000, layout=1, seed_a=83, seed_b=84),
+             inputs.make_problem("fly", "bf16", 3000, 1100, 500, seed_a=85, seed_b=86)]
+    host = [(p.a.pin_memory(), p.b.pin_memory()) for p in probs]
+    bufs = [{} for _ in probs]
+    pending = [gemm.matmul_from_host(a, b, layout=p.layout, buffers=bf, wait=False)
+               for (a, b), p, bf in zip(host, probs, bufs)]
+    for (C, done), p in zip(pending, probs):
+        done.synchronize()
+        _check_full(p, C)
+    # same buffers, other operands of the same shapes: the second call waits for the first
+    q = inputs.make_problem("fly", "tf32", 1500, 900, 700, seed_a=87, seed_b=88)
+    first, _ = gemm.matmul_from_host(*host[0], buffers=bufs[0], wait=False)
+    C, done = gemm.matmul_from_host(q.a.pin_memory(), q.b.pin_memory(), buffers=bufs[0], wait=False)
+    done.synchronize()
+    assert C.data_ptr() == first.data_ptr()  # one pinned result per buffers dict
+    _check_full(q, C)
+
+
 @pytest.mark.parametrize("dtype,shape", [
     ("bf16", (256, 200, 1 << 18)),     # 2048 k-slabs: long accumulation, split segments of hundreds of slabs
     ("tf32", (130, 260, 1 << 16)),
