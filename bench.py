@@ -284,10 +284,15 @@ KIND_INDEX = {"f16": 0, "bf16": 1, "tf32": 2}
 
 
 def kernel_name(dtype, plan):
-    """The product kernel a plan launches, as ncu names it (row-major B)."""
+    """The product kernel a plan launches, as ncu names it (row-major B).
+    Plan kernel 1: single CTA; 2 and 4: one or two CTA pairs per cluster
+    (operand arrangement 0); 3: a CTA pair on the transposed product
+    (arrangement 2)."""
     k, bn = plan["kernel"], plan["tile_n"]
     if k == 1:
         return f"gemm_kernel<{KIND_INDEX[dtype]}, 0, {bn}>"
+    if k == 3:
+        return f"gemm_kernel_pair<{KIND_INDEX[dtype]}, 2, {bn}, 1>"
     return f"gemm_kernel_pair<{KIND_INDEX[dtype]}, 0, {bn}, {k // 2}>"
 
 

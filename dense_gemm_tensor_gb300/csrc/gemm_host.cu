@@ -325,6 +325,7 @@ struct TilePlan {
   int grid;   // CTAs
   int segs;   // pair kernel: k-slab segments per tile of the last partial round (1 = no split)
   int conc;   // tiles in flight at once (SMs, or co-resident CTA pairs)
+  bool swap;  // pair kernel on the transposed product C^T = B^T A^T (row-major B)
 };
 
 // Cycles one SM spends per 128-byte k-slab of a tile in the steady state of
@@ -340,8 +341,21 @@ constexpr double kSlabCycles[3][4] = {
     {560.0, 503.0, 500.0, 470.0},  // two pairs sharing A, two 256 x width tiles
 };
 // TF32 with row-major B fetches B in 32-column boxes, twice as many as the
-// 16-bit kinds; its pair and shared-A slabs measured 564/542/495/476 cycles.
-constexpr double kSlabCyclesTf32Mn[4] = {564.0, 542.0, 495.0, 476.0};
+// 16-bit kinds; its pair and shared-A slabs measured 564/542/495/476 cycles,
+// the 224-wide one since recalibrated against the 256-wide one by their times
+// at 4096^3 (158.2 and 157.2 us with K walked in alternating directions).
+constexpr double kSlabCyclesTf32Mn[4] = {564.0, 512.0, 495.0, 476.0};
+// The pair kernel on the transposed product (row-major B as the MMA's A
+// operand, in whole 128-byte boxes): its stages hold no unused columns, so
+// widths 224 and 192 keep seven stages, which outweighs its costlier
+// epilogue (a transpose on the way to shared memory) at 224 and not at 256.
+// Scaled from the plain pair's table by the times measured at 4096^3
+// (16-bit: 224-wide 82.6 against 84.4 us, 256-wide 89.6 against 87.3 us,
+// 192-wide 97.0 us over five rounds; TF32: 154.9 against 158.2 us, 160.6
+// against 157.2 us, 192-wide 177.5 us); the 128-wide entries (not measured)
+// are the plain pair's with the 256-wide penalty.
+constexpr double kSlabCyclesSwap[4] = {579.0, 493.0, 467.0, 476.0};
+constexpr double kSlabCyclesSwapTf32[4] = {576.0, 501.0, 461.0, 488.0};
 
 // Picks the kernel (single CTA, CTA pair, or two pairs sharing A), the tile
 // width and the tile order.
@@ -357,26 +371,36 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
   const int fv = g_force_variant.load(std::memory_order_relaxed);
   const int fb = g_force_bn.load(std::memory_order_relaxed);
   const int fr = g_force_raster.load(std::memory_order_relaxed);
-  TilePlan best{false, 1, 256, 8, sms, 1, sms};
+  TilePlan best{false, 1, 256, 8, sms, 1, sms, false};
   double best_cost = -1.0;
-  auto consider = [&](bool pair, int pairs, int bn) {
+  // the transposed product: C's columns take the 256-row side of the pair's tile
+  const bool swap_ok = !kmajor && (kind == KIND_TF32 || kind == KIND_F16 || kind == KIND_BF16);
+  auto consider = [&](bool pair, int pairs, int bn, bool swap) {
     if (fv == 1 && pair) return;
-    if (fv == 2 && !(pair && pairs == 1)) return;
+    if (fv == 2 && !(pair && pairs == 1 && !swap)) return;
     if (fv == 3 && !(pair && pairs == 2)) return;
+    if (fv == 4 && !swap) return;
     if (fb && fb != bn) return;
     if (pair && !all_tma) return;
+    if (swap && !(swap_ok && pair && pairs == 1)) return;
+    // extents of the tile grid: the MMA's A side (256-row pair tiles) and its B side (bn wide)
+    const int64_t ma = swap ? N : M, nb_ext = swap ? M : N;
     int conc;  // work tiles in flight
     if (pair) {
+      // (the transposed product's kernel has the same cluster shape and one CTA per SM)
       conc = pair_clusters(dev, kind, kmajor, bn, pairs);
       if (conc <= 0) return;
     } else {
       conc = sms;
     }
     const int wi = bn == 256 ? 0 : bn == 224 ? 1 : bn == 192 ? 2 : 3;
-    const double slab = (pair && kind == KIND_TF32 && !kmajor) ? kSlabCyclesTf32Mn[wi] : kSlabCycles[pair ? pairs : 0][wi];
+    const double slab = swap                                     ? (kind == KIND_TF32 ? kSlabCyclesSwapTf32[wi]
+                                                                                      : kSlabCyclesSwap[wi])
+                        : (pair && kind == KIND_TF32 && !kmajor) ? kSlabCyclesTf32Mn[wi]
+                                                                 : kSlabCycles[pair ? pairs : 0][wi];
     const int64_t rows = pair ? 256 : 128;
-    const int64_t tiles_n = (N + bn - 1) / bn;
-    const int64_t tiles = nbat * ((M + rows - 1) / rows) * ((tiles_n + pairs - 1) / pairs);
+    const int64_t tiles_n = (nb_ext + bn - 1) / bn;
+    const int64_t tiles = nbat * ((ma + rows - 1) / rows) * ((tiles_n + pairs - 1) / pairs);
     const int64_t full = tiles / conc, rest = tiles % conc;
     // pair kernel: the tiles of the last partial round may be split along K
     // into `segs` pieces run by different pairs (fp32 partials summed at the end)
@@ -400,7 +424,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
     }
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
-      const int64_t tiles_m = (M + rows - 1) / rows;
+      const int64_t tiles_m = (ma + rows - 1) / rows;
       const int64_t work = tiles + (segs - 1) * rest;
       const int64_t grid_tiles = work < conc ? work : conc;
       // band height: 2 pair rows / 8 single-CTA rows (measured best at 4096^3) while
@@ -408,21 +432,22 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
       // as many rows as keep the band's A rows within ~40 MB of L2
       const int band_min = pair ? 2 : 8;
       int band = band_min;
-      if (double(K) * double(N) * es > 64.0e6) {
+      if (double(K) * double(nb_ext) * es > 64.0e6) {
         band = int(40.0e6 / (double(rows) * double(K) * es));
         if (band < band_min) band = band_min;
         if (band > 16) band = 16;
       }
       best = TilePlan{pair, pairs, bn, int(tiles_m < band ? tiles_m : band),
-                      int(pair ? 2 * pairs * grid_tiles : grid_tiles), segs, conc};
+                      int(pair ? 2 * pairs * grid_tiles : grid_tiles), segs, conc, swap};
     }
   };
-  for (int bn : kPairTileWidths) consider(true, 2, bn);
-  for (int bn : kPairTileWidths) consider(true, 1, bn);
-  for (int bn : kTileWidths) consider(false, 1, bn);
+  for (int bn : kPairTileWidths) consider(true, 2, bn, false);
+  for (int bn : kPairTileWidths) consider(true, 1, bn, false);
+  for (int bn : kPairTileWidths) consider(true, 1, bn, true);
+  for (int bn : kTileWidths) consider(false, 1, bn, false);
   if (best_cost < 0) {  // a forced combination that does not apply: fall back to the single-CTA default
     const int64_t tiles = nbat * ((M + 127) / 128) * ((N + 255) / 256);
-    best = TilePlan{false, 1, 256, 8, int(tiles < sms ? tiles : sms), 1, sms};
+    best = TilePlan{false, 1, 256, 8, int(tiles < sms ? tiles : sms), 1, sms, false};
   }
   if (fr) best.raster = fr;
   return best;
@@ -593,8 +618,9 @@ int prepare(const Call& c, const DeviceInfo* dev, int dev_id, TilePlan& plan, Op
   const int64_t b_rows = op.kmajor ? N : K, b_cols = op.kmajor ? K : N;  // of the operand the kernel reads
   const int64_t ldb_p = pack_b ? (b_cols * es + 127) / 128 * 128 / es : c.ldb;
   auto split_tiles = [&](const TilePlan& pl) {
-    const int64_t tm = (M + (pl.pair ? 255 : 127)) / (pl.pair ? 256 : 128);
-    const int64_t tn = ((N + pl.bn - 1) / pl.bn + pl.pairs - 1) / pl.pairs;
+    const int64_t ma = pl.swap ? N : M, nb_ext = pl.swap ? M : N;
+    const int64_t tm = (ma + (pl.pair ? 255 : 127)) / (pl.pair ? 256 : 128);
+    const int64_t tn = ((nb_ext + pl.bn - 1) / pl.bn + pl.pairs - 1) / pl.pairs;
     const int64_t r = (pl.pair && pl.segs > 1) ? (nbat * tm * tn) % pl.conc : 0;
     return (r > 0 && r <= 1024) ? int(r) : 0;
   };
@@ -621,9 +647,10 @@ int prepare(const Call& c, const DeviceInfo* dev, int dev_id, TilePlan& plan, Op
   }
   // work decomposition: tiles along N count pairs of adjacent tiles for the
   // shared-A kernel (the second past the last column when the count is odd:
-  // computed, not stored)
-  const int64_t tiles_m = (M + (plan.pair ? 255 : 127)) / (plan.pair ? 256 : 128);
-  const int64_t tiles_n = ((N + plan.bn - 1) / plan.bn + plan.pairs - 1) / plan.pairs;
+  // computed, not stored); the transposed product tiles C^T (N x M)
+  const int64_t ma = plan.swap ? N : M, nb_ext = plan.swap ? M : N;
+  const int64_t tiles_m = (ma + (plan.pair ? 255 : 127)) / (plan.pair ? 256 : 128);
+  const int64_t tiles_n = ((nb_ext + plan.bn - 1) / plan.bn + plan.pairs - 1) / plan.pairs;
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
@@ -685,13 +712,18 @@ int encode_maps(const Call& c, const TilePlan& plan, const Operands& op, LaunchP
   const uint32_t bk = 128 / es;  // K elements per 128-byte row
   const uint64_t za = p.stride_a ? nbat : 1, zb = p.stride_b ? nbat : 1;
   const uint64_t M = uint64_t(c.M), N = uint64_t(c.N), K = uint64_t(c.K);
-  // A box: 128 rows, or 64 where two pairs each load half a CTA's rows for both
-  if (p.a_tma && !encode_3d(&L.tmA, dt, op.A, K, M, uint64_t(op.lda) * es, za, uint64_t(p.stride_a) * es, bk,
-                            (plan.pair && plan.pairs == 2) ? 64 : 128))
+  // A box: 128 rows, or 64 where two pairs each load half a CTA's rows for
+  // both, or (transposed product) the bn / 2 rows of C a CTA computes
+  const uint32_t a_rows = plan.swap ? uint32_t(bn / 2) : (plan.pair && plan.pairs == 2) ? 64u : 128u;
+  if (p.a_tma && !encode_3d(&L.tmA, dt, op.A, K, M, uint64_t(op.lda) * es, za, uint64_t(p.stride_a) * es, bk, a_rows))
     return GEMM_ERR_DRIVER;
   if (p.b_tma) {
     bool ok;
-    if (op.kmajor) {
+    if (plan.swap) {
+      // B^T as the MMA's MN-major A operand: whole 128-byte boxes of 128 / es columns
+      const CUtensorMapSwizzle swz = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+      ok = encode_3d(&L.tmB, dt, op.B, N, K, uint64_t(op.ldb) * es, zb, uint64_t(p.stride_b) * es, 128 / es, bk, swz);
+    } else if (op.kmajor) {
       ok = encode_3d(&L.tmB, dt, op.B, K, N, uint64_t(op.ldb) * es, zb, uint64_t(p.stride_b) * es, bk,
                      uint32_t(plan.pair ? bn / 2 : bn));
     } else {
@@ -789,6 +821,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   if (st != GEMM_OK) return st;
   L.b_kmajor = op.kmajor;
   L.pair = plan.pair;
+  L.swap = plan.swap;
   L.pairs = plan.pairs;
   L.bn = plan.bn;
   L.grid = plan.grid;
@@ -801,17 +834,19 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
       p.tiles_m < 1 || (L.pair && L.pairs != 1 && L.pairs != 2) || (!L.pair && L.pairs != 1))
     return GEMM_ERR_LAUNCH;
   if (c.fp8 && !(p.a_tma && p.b_tma && op.kmajor)) return GEMM_ERR_LAUNCH;  // guaranteed by prepare()
+  if (L.swap && !(L.pair && L.pairs == 1 && !op.kmajor && !c.fp8)) return GEMM_ERR_LAUNCH;  // choose_plan's rule
   cudaError_t e;
   switch (kind) {
-    case KIND_TF32: e = op.kmajor ? launch_tf32_km(L) : launch_tf32_rm(L); break;
-    case KIND_BF16: e = op.kmajor ? launch_bf16_km(L) : launch_bf16_rm(L); break;
-    case KIND_F16: e = op.kmajor ? launch_f16_km(L) : launch_f16_rm(L); break;
+    case KIND_TF32: e = L.swap ? launch_tf32_sw(L) : op.kmajor ? launch_tf32_km(L) : launch_tf32_rm(L); break;
+    case KIND_BF16: e = L.swap ? launch_bf16_sw(L) : op.kmajor ? launch_bf16_km(L) : launch_bf16_rm(L); break;
+    case KIND_F16: e = L.swap ? launch_f16_sw(L) : op.kmajor ? launch_f16_km(L) : launch_f16_rm(L); break;
     case KIND_E4M3: e = launch_e4m3_km(L); break;
     default: e = launch_e5m2_km(L); break;
   }
   if (e != cudaSuccess) return GEMM_ERR_LAUNCH;
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  const int32_t info[8] = {plan.pair ? 2 * plan.pairs : 1, plan.bn, p.raster, L.grid, p.tail_segs, plan.conc,
+  const int32_t info[8] = {plan.swap ? 3 : plan.pair ? 2 * plan.pairs : 1, plan.bn, p.raster, L.grid, p.tail_segs,
+                           plan.conc,
                            p.tail_start, p.num_work};
   memcpy(t_last_plan, info, sizeof(info));
   return GEMM_OK;
@@ -1016,7 +1051,7 @@ int gemm_last_plan(int32_t* out) {
 }
 
 int gemm_set_tuning(int variant, int tile_n, int raster, int tail_split) {
-  if (variant < 0 || variant > 3 || raster < 0 || tail_split < 0 || tail_split > 2) return GEMM_ERR_INVALID_VALUE;
+  if (variant < 0 || variant > 4 || raster < 0 || tail_split < 0 || tail_split > 2) return GEMM_ERR_INVALID_VALUE;
   if (tile_n != 0) {
     bool ok = false;
     if (variant < 2)

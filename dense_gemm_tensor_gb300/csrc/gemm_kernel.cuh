@@ -644,6 +644,116 @@ __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMa
   }
 }
 
+// Address of the element at byte `byte` (0 .. 63) of row r of a staging tile.
+__device__ __forceinline__ uint32_t epi_elem_addr(uint32_t stage, int r, int byte) {
+  return epi_chunk_addr(stage, r, byte >> 4) + static_cast<uint32_t>(byte & 15);
+}
+
+// A staged element of the output type, as float.
+template <int KIND>
+__device__ __forceinline__ float epi_load_elem(uint32_t addr) {
+  if constexpr (KIND == KIND_TF32) {
+    return __uint_as_float(ld_shared_u32(addr));
+  } else if constexpr (KIND == KIND_BF16) {
+    return __uint_as_float(ld_shared_u16(addr) << 16);
+  } else {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(ld_shared_u16(addr))));
+  }
+}
+
+// emit_chunk_t with the fused epilogue: each lane computes its column's 32
+// values (alpha * acc, beta * C, bias[col], activation: the order of
+// epi_round_fused) and stores them element by element.
+template <int KIND>
+__device__ __forceinline__ void emit_chunk_t_fused(const GemmParams& p, const CUtensorMap* tmC, EpiRing& ring, int lane,
+                                                int row0, int col0, int bz, const uint32_t (&r)[32]) {
+  constexpr int ES = KIND == KIND_TF32 ? 4 : 2;
+  constexpr int RC = 64 / ES;  // columns per staging tile
+  using T = typename KindTraits<KIND>::T;
+  float bias = 0.0f;
+  const bool has_bias = p.bias != nullptr && col0 + lane < p.N;
+  if (has_bias) {
+    const T b = static_cast<const T*>(p.bias)[col0 + lane];
+    if constexpr (KIND == KIND_TF32)
+      bias = b;
+    else if constexpr (KIND == KIND_BF16)
+      bias = __bfloat162float(b);
+    else
+      bias = __half2float(b);
+  }
+  for (int h = 0; h < 32 / RC; ++h) {
+    const int cb = col0 + h * RC;
+    if (cb >= p.N) break;
+    const uint32_t stage = epi_acquire(p, lane, ring);
+    if (p.beta != 0.0f) epi_load_c<KIND>(p, stage, lane, row0, cb, bz);
+    if (lane / RC == h) {
+      const int byte = (lane - h * RC) * ES;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t a = epi_elem_addr(stage, j, byte);
+        float v = p.alpha * __uint_as_float(r[j]);
+        if (p.beta != 0.0f) v += p.beta * epi_load_elem<KIND>(a);
+        if (has_bias) v += bias;
+        v = epi_activation(v, p.act);
+        if constexpr (KIND == KIND_TF32)
+          st_shared_u32(a, __float_as_uint(v));
+        else
+          st_shared_u16(a, pack2<KIND>(__float_as_uint(v), 0u) & 0xFFFFu);
+      }
+    }
+    epi_flush<KIND>(p, tmC, stage, lane, row0, cb, bz);
+  }
+}
+
+// emit_chunk for an accumulator that holds a tile of C^T: lane l has
+// C[row0 + j][col0 + l] in r[j], j = 0..31 (32 rows of one column of C per
+// lane). Each staging tile is a 32-row box of C; neighbouring lanes trade a
+// value so that each stores whole 32-bit words, a pair of rows per step (one
+// lane row j, its partner row j + 1), 128 bytes a step for the warp, free of
+// bank conflicts. 16-bit C: lanes 2i and 2i+1 hold columns 2i and 2i+1 and
+// write the word of that column pair in rows j and j+1. fp32 C (two tiles of
+// 16 columns): lanes l and l ^ 16 trade their row-(j+1) values, so in the
+// tile of the lower 16 columns lanes 0-15 write row j and lanes 16-31 row
+// j + 1, and the other way round in the upper tile. The tile then leaves as
+// in emit_chunk. Warp-collective.
+template <int KIND>
+__device__ __forceinline__ void emit_chunk_t(const GemmParams& p, const CUtensorMap* tmC, EpiRing& ring, int lane,
+                                             int row0, int col0, int bz, const uint32_t (&r)[32]) {
+  if (p.fused) {
+    emit_chunk_t_fused<KIND>(p, tmC, ring, lane, row0, col0, bz, r);
+    return;
+  }
+  if constexpr (KIND == KIND_TF32) {
+    const int k = (lane & 15) * 4;  // byte of this lane's column within a tile
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int cb = col0 + 16 * h;
+      if (cb >= p.N) break;
+      const uint32_t stage = epi_acquire(p, lane, ring);
+      const bool own = (lane >> 4) == h;  // this lane's column lies in tile h
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, r[2 * i + 1], 16);  // partner's row 2i+1
+        st_shared_u32(epi_elem_addr(stage, 2 * i + (own ? 0 : 1), k), own ? r[2 * i] : y);
+      }
+      epi_flush<KIND>(p, tmC, stage, lane, row0, cb, bz);
+    }
+  } else {
+    if (col0 >= p.N) return;
+    const bool odd = lane & 1;
+    const int k = (lane >> 1) * 4;  // byte of this lane's column pair within the tile
+    const uint32_t stage = epi_acquire(p, lane, ring);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t x = odd ? r[2 * i] : r[2 * i + 1];
+      const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+      const uint32_t w = odd ? pack2<KIND>(y, r[2 * i + 1]) : pack2<KIND>(r[2 * i], y);
+      st_shared_u32(epi_elem_addr(stage, 2 * i + (odd ? 1 : 0), k), w);
+    }
+    epi_flush<KIND>(p, tmC, stage, lane, row0, col0, bz);
+  }
+}
+
 // Reads `nchunks` 32-column chunks of this warp's 32 accumulator rows from
 // tensor memory and hands each to `use(c, r)`, keeping the next chunk's load
 // in flight while the current one is used. Warp-collective.

@@ -38,30 +38,51 @@
 
 namespace dgt {
 
-template <int KIND, bool B_KMAJOR, int BN_>
+// Operand arrangements of the pair kernel (its OPS parameter).
+enum : int {
+  OPS_B_MN = 0,  // A K-major (row-major M x K), B MN-major (row-major K x N)
+  OPS_B_K = 1,   // A and B K-major (B given as N x K)
+  // The transposed product C^T = B^T A^T for a row-major B: the MMA's A operand
+  // is B^T, MN-major, 128 of C's columns per CTA in whole 128-byte boxes; its B
+  // operand is A, K-major, BN / 2 of C's rows per CTA; the accumulator holds
+  // a tile of C^T (tensor-memory lane = column of C, column = row of C). A tile
+  // width that is not whole 128-byte boxes of B (224, 192) then costs no
+  // unused shared memory, and the 224-wide tile gets a seventh stage.
+  OPS_SWAP = 2,
+};
+
+template <int KIND, int OPS, int BN_>
 struct PairCfg {
   using T = typename KindTraits<KIND>::T;
+  static constexpr bool B_KMAJOR = OPS == OPS_B_K;
+  static constexpr bool SWAP = OPS == OPS_SWAP;
   static constexpr int ES = sizeof(T);
-  static constexpr int BM = 128;   // rows per CTA
-  static constexpr int BMP = 256;  // rows per pair
-  static constexpr int BN = BN_;   // tile width (columns of the pair's tile)
+  static constexpr int BM = 128;   // rows of the MMA's A operand per CTA (of C^T when SWAP)
+  static constexpr int BMP = 256;  // per pair
+  static constexpr int BN = BN_;   // tile width (columns of the pair's accumulator; rows of C when SWAP)
   static constexpr int BNH = BN / 2;
   static constexpr int BK = 128 / ES;
   static constexpr int UK = 32 / ES;
   static constexpr int KSTEPS = BK / UK;
-  static constexpr int A_BYTES = BM * 128;
+  // MN-major boxes (B, or B^T as the MMA's A operand when SWAP): 128-byte rows along M/N
   static constexpr int BOXN = 128 / ES;
-  static constexpr int NBOX = (BNH + BOXN - 1) / BOXN;  // MN-major B: boxes per CTA (last may be partly used)
   static constexpr int BOX_BYTES = BK * 128;
-  static constexpr int B_BYTES = B_KMAJOR ? BNH * 128 : NBOX * BOX_BYTES;
+  static constexpr bool MN_ATOM32 = ES == 4;  // fp32 MN-major: 128-byte swizzle of 32-byte chunks
+  static constexpr uint32_t MN_SWZ = MN_ATOM32 ? SWZ_128B_ATOM32 : SWZ_128B;
+  static constexpr uint32_t MN_SBO = MN_ATOM32 ? DGT_ATOM32_SBO : 1024;
+  static constexpr int A_BYTES = BM * 128;  // 128 K-major rows, or (SWAP) 128 / BOXN MN-major boxes
+  static constexpr int NABOX = SWAP ? BM / BOXN : 0;
+  static constexpr int NBOX = (BNH + BOXN - 1) / BOXN;  // MN-major B: boxes per CTA (last may be partly used)
+  static constexpr int B_BYTES = (B_KMAJOR || SWAP) ? BNH * 128 : NBOX * BOX_BYTES;
   // MN-major B: the last box carries only the columns the tile uses (a
   // narrower box still lands in 128-byte swizzled rows), so a stage moves
   // B_TX bytes of B while taking B_BYTES of shared memory.
   static constexpr int LASTN = BNH - (NBOX - 1) * BOXN;
-  static constexpr int B_TX = B_KMAJOR ? B_BYTES : (NBOX - 1) * BOX_BYTES + LASTN * BK * ES;
-  static constexpr bool B_ATOM32 = (ES == 4) && !B_KMAJOR;
-  static constexpr uint32_t B_SWZ = B_ATOM32 ? SWZ_128B_ATOM32 : SWZ_128B;
-  static constexpr uint32_t B_SBO = B_ATOM32 ? DGT_ATOM32_SBO : 1024;
+  static constexpr bool B_MN = OPS == OPS_B_MN;
+  static constexpr int B_TX = B_MN ? (NBOX - 1) * BOX_BYTES + LASTN * BK * ES : B_BYTES;
+  static constexpr bool B_ATOM32 = MN_ATOM32 && B_MN;
+  static constexpr uint32_t B_SWZ = MN_SWZ;
+  static constexpr uint32_t B_SBO = MN_SBO;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGE_TX = A_BYTES + B_TX;  // bytes the TMA loads of one CTA's stage deliver
   static constexpr int SMEM_LIMIT = 232448;
@@ -77,13 +98,15 @@ struct PairCfg {
   static constexpr int PARTIAL_FLOATS = BM * BN;  // one CTA's fp32 partial tile
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
   static_assert(BNH % 16 == 0, "each CTA's B half is whole 16-column groups");
+  static_assert(!SWAP || BM % BOXN == 0, "B^T comes in whole boxes");
   static_assert(ACC_BUFS * BN <= 512, "tensor memory");
   static_assert(NUM_BARS * 8 + 32 <= 256, "barrier area");
   static_assert(STAGES >= 3, "pipeline depth");
   static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
+  // bit 15: A MN-major (SWAP), bit 16: B MN-major (row-major B, not swapped)
   static constexpr uint32_t IDESC = (1u << 4) | (KindTraits<KIND>::fmt << 7) | (KindTraits<KIND>::fmt << 10) |
-                                    ((B_KMAJOR ? 0u : 1u) << 16) | (uint32_t(BN >> 3) << 17) |
-                                    (uint32_t(BMP >> 4) << 24);
+                                    ((SWAP ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+                                    (uint32_t(BN >> 3) << 17) | (uint32_t(BMP >> 4) << 24);
 };
 
 // Work item w of the pair kernel -> tile, k-slab range and (for split tiles)
@@ -136,16 +159,18 @@ __device__ __forceinline__ int pair_kb(const PairWork& wk, int i, int round) {
 
 __device__ __forceinline__ void epilogue_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-template <int KIND, bool B_KMAJOR, int BN, int PAIRS>
+template <int KIND, int OPS, int BN, int PAIRS>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
                      const GemmParams p) {
-  using Cf = PairCfg<KIND, B_KMAJOR, BN>;
+  using Cf = PairCfg<KIND, OPS, BN>;
+  constexpr bool B_KMAJOR = Cf::B_KMAJOR;
   constexpr int S = Cf::STAGES;
   constexpr int NB = Cf::ACC_BUFS;
   constexpr int CL = 2 * PAIRS;  // CTAs per cluster
   static_assert(PAIRS == 1 || PAIRS == 2, "one pair, or two pairs sharing A");
+  static_assert(PAIRS == 1 || !Cf::SWAP, "the transposed product runs as single pairs");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -191,7 +216,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (!B_KMAJOR && Cf::LASTN != Cf::BOXN) tma_prefetch_desc(&tmB2);
+    if (Cf::B_MN && Cf::LASTN != Cf::BOXN) tma_prefetch_desc(&tmB2);
   }
   if (warp == 5) {
     tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), Cf::TMEM_COLS);
@@ -214,6 +239,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int w = pair; ok && w < p.num_work; w += npairs, ++tc) {
         const PairWork wk = pair_work(p, w);
+        // rows of the MMA's A operand (SWAP: columns of C) and columns of its B operand (SWAP: rows of C)
         const int row0 = wk.mb * Cf::BMP + int(half) * Cf::BM;
         const int col0 = (wk.nb * PAIRS + q) * BN + int(half) * Cf::BNH;
         const int za = p.stride_a ? wk.bz : 0, zb = p.stride_b ? wk.bz : 0;  // a stride of 0 repeats matrix 0
@@ -230,24 +256,34 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b_dst = sB + s * Cf::B_BYTES;
           const bool ld_ok = in_range(p, s < S && a_dst + Cf::A_BYTES <= sB, CHECK_A_STAGE) &&
                              in_range(p, b_dst + Cf::B_BYTES <= sE, CHECK_B_STAGE) &&
-                             in_range(p, (kb * Cf::BK * Cf::ES) % 16 == 0 && (col0 * Cf::ES) % 16 == 0, CHECK_TMA_X);
+                             in_range(p, (kb * Cf::BK * Cf::ES) % 16 == 0 && ((Cf::SWAP ? row0 : col0) * Cf::ES) % 16 == 0,
+                                      CHECK_TMA_X);
           if (ld_ok && elect_one()) {
             if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * Cf::STAGE_TX);
-            if constexpr (PAIRS == 1) {
-              tma_load_3d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0, za);
-            } else {
-              // both pairs need these 128 rows of A: each loads 64 of them into
-              // the same place in its own and the other pair's CTA of this half
-              tma_load_3d_pair_mc(a_dst + q * (Cf::A_BYTES / 2), &tmA, fb, kb * Cf::BK, row0 + q * (Cf::BM / 2),
-                                  za, uint16_t(0x5u << half));
-            }
-            if constexpr (B_KMAJOR) {
-              tma_load_3d_pair(b_dst, &tmB, fb, kb * Cf::BK, col0, zb);
-            } else {
+            if constexpr (Cf::SWAP) {
+              // B^T: this CTA's 128 columns of C in MN-major boxes; A: its BN / 2 rows of C, K-major
 #pragma unroll
-              for (int j = 0; j < Cf::NBOX; ++j)
-                tma_load_3d_pair(b_dst + j * Cf::BOX_BYTES, (j == Cf::NBOX - 1 && Cf::LASTN != Cf::BOXN) ? &tmB2 : &tmB,
-                                 fb, col0 + j * Cf::BOXN, kb * Cf::BK, zb);
+              for (int j = 0; j < Cf::NABOX; ++j)
+                tma_load_3d_pair(a_dst + j * Cf::BOX_BYTES, &tmB, fb, row0 + j * Cf::BOXN, kb * Cf::BK, zb);
+              tma_load_3d_pair(b_dst, &tmA, fb, kb * Cf::BK, col0, za);
+            } else {
+              if constexpr (PAIRS == 1) {
+                tma_load_3d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0, za);
+              } else {
+                // both pairs need these 128 rows of A: each loads 64 of them into
+                // the same place in its own and the other pair's CTA of this half
+                tma_load_3d_pair_mc(a_dst + q * (Cf::A_BYTES / 2), &tmA, fb, kb * Cf::BK, row0 + q * (Cf::BM / 2),
+                                    za, uint16_t(0x5u << half));
+              }
+              if constexpr (B_KMAJOR) {
+                tma_load_3d_pair(b_dst, &tmB, fb, kb * Cf::BK, col0, zb);
+              } else {
+#pragma unroll
+                for (int j = 0; j < Cf::NBOX; ++j)
+                  tma_load_3d_pair(b_dst + j * Cf::BOX_BYTES,
+                                   (j == Cf::NBOX - 1 && Cf::LASTN != Cf::BOXN) ? &tmB2 : &tmB, fb,
+                                   col0 + j * Cf::BOXN, kb * Cf::BK, zb);
+              }
             }
           }
           __syncwarp();
@@ -286,8 +322,11 @@ __global__ void __launch_bounds__(192, 1)
           uint64_t ad[Cf::KSTEPS], bd[Cf::KSTEPS];
 #pragma unroll
           for (int kk = 0; kk < Cf::KSTEPS; ++kk) {
-            ad[kk] = sdesc(a_addr + kk * 32, 16, 1024, SWZ_128B);
-            if constexpr (B_KMAJOR)
+            if constexpr (Cf::SWAP)
+              ad[kk] = sdesc(a_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::MN_SBO, Cf::MN_SWZ);
+            else
+              ad[kk] = sdesc(a_addr + kk * 32, 16, 1024, SWZ_128B);
+            if constexpr (B_KMAJOR || Cf::SWAP)
               bd[kk] = sdesc(b_addr + kk * 32, 16, 1024, SWZ_128B);
             else
               bd[kk] = sdesc(b_addr + kk * Cf::UK * 128, Cf::BOX_BYTES, Cf::B_SBO, Cf::B_SWZ);
@@ -331,15 +370,23 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok_slot[tc & 1]) break;
       tc_fence_after();
       const int nbt = wk.nb * PAIRS + q;  // this pair's tile column (past the last one: nothing to store)
-      const int row0 = wk.mb * Cf::BMP + int(half) * Cf::BM + warp * 32;  // first of this warp's 32 rows
+      // first of this warp's 32 accumulator rows (SWAP: columns of C), and the
+      // tile's first accumulator column (SWAP: row of C)
+      const int row0 = wk.mb * Cf::BMP + int(half) * Cf::BM + warp * 32;
+      const int col0 = nbt * BN;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
-      const int ncols = min(BN, p.N - nbt * BN);
+      const int ncols = min(BN, (Cf::SWAP ? p.M : p.N) - col0);
       int nchunks = ncols > 0 ? (ncols + 31) / 32 : 0;
       if (!in_range(p, b * Cf::ACC_COLS + nchunks * 32 <= Cf::TMEM_COLS, CHECK_TMEM_LD)) nchunks = 0;
-      const int col0 = nbt * BN;
+      // accumulator chunk c (32 columns) of the warp's 32 rows, as output
+      auto emit = [&](int c, const uint32_t(&v)[32]) {
+        if constexpr (Cf::SWAP)
+          emit_chunk_t<KindTraits<KIND>::out>(p, &tmC, ring, lane, col0 + c * 32, row0, wk.bz, v);
+        else
+          emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, v);
+      };
       if (wk.f < 0) {
-        for_each_acc_chunk(taddr, nchunks,
-                           [&](int c, const uint32_t(&r)[32]) { emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, r); });
+        for_each_acc_chunk(taddr, nchunks, emit);
       } else {
         // split tile: publish this segment's partial, then find out whether it is the last
         // (every slot this tile's segments use, and its counters, lie in the scratch)
@@ -388,7 +435,7 @@ __global__ void __launch_bounds__(192, 1)
               sum[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + cur[q].z);
               sum[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + cur[q].w);
             }
-            emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, sum);
+            emit(c, sum);
           });
         } else if (last) {
           // three or four segments: add them in segment order; this CTA's own one comes from tensor memory
@@ -417,7 +464,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t out[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) out[j] = __float_as_uint(acc[j]);
-            emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, out);
+            emit(c, out);
           });
         }
       }

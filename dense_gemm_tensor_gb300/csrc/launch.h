@@ -17,6 +17,7 @@ struct LaunchPlan {
   GemmParams p;
   bool b_kmajor;
   bool pair;  // CTA-pair kernel (cta_group::2)
+  bool swap;  // pair kernel on the transposed product (row-major B; OPS_SWAP)
   int pairs;  // pair kernel: CTA pairs per cluster (1, or 2 sharing A by multicast)
   int bn;     // output tile width: one of kTileWidths (single) or kPairTileWidths (pair)
   int grid;
@@ -40,6 +41,10 @@ DGT_DECLARE_VARIANTS(tf32_km)
 DGT_DECLARE_VARIANTS(e4m3_km)
 DGT_DECLARE_VARIANTS(e5m2_km)
 #undef DGT_DECLARE_VARIANTS
+// The pair kernel on the transposed product (row-major B), one unit per kind.
+cudaError_t launch_f16_sw(const LaunchPlan& L);
+cudaError_t launch_bf16_sw(const LaunchPlan& L);
+cudaError_t launch_tf32_sw(const LaunchPlan& L);
 cudaError_t launch_fill_zero(void* C, long long ldc, int M, int N, int es, cudaStream_t stream, int sm_count);
 // dst[n][k] = src[k][n] for a rows x cols byte matrix (leading dimensions in bytes).
 cudaError_t launch_transpose_bytes(const void* src, int64_t src_ld, void* dst, int64_t dst_ld, int64_t rows,
@@ -114,14 +119,14 @@ cudaError_t launch_layout(const LaunchPlan& L) {
 }
 
 
-template <int KIND, bool KMAJ, int BN, int PAIRS>
+template <int KIND, int OPS, int BN, int PAIRS>
 cudaError_t launch_pair_variant(const LaunchPlan& L) {
   static int configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_kernel_pair<KIND, KMAJ, BN, PAIRS>;
-  constexpr int smem = PairCfg<KIND, KMAJ, BN>::SMEM_BYTES;
+  auto kern = gemm_kernel_pair<KIND, OPS, BN, PAIRS>;
+  constexpr int smem = PairCfg<KIND, OPS, BN>::SMEM_BYTES;
   if (dev >= 64 || !__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -150,10 +155,10 @@ cudaError_t launch_pair_variant(const LaunchPlan& L) {
 }
 
 // Co-resident clusters of one pair variant (occupancy query with its launch shape).
-template <int KIND, bool KMAJ, int BN, int PAIRS>
+template <int KIND, int OPS, int BN, int PAIRS>
 int pair_clusters_variant() {
-  auto kern = gemm_kernel_pair<KIND, KMAJ, BN, PAIRS>;
-  constexpr int smem = PairCfg<KIND, KMAJ, BN>::SMEM_BYTES;
+  auto kern = gemm_kernel_pair<KIND, OPS, BN, PAIRS>;
+  constexpr int smem = PairCfg<KIND, OPS, BN>::SMEM_BYTES;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -177,46 +182,54 @@ int pair_clusters_variant() {
   return n;
 }
 
-template <int KIND, bool KMAJ, int PAIRS>
+template <int KIND, int OPS, int PAIRS>
 cudaError_t launch_pair_width(const LaunchPlan& L) {
   switch (L.bn) {
-    case 256: return launch_pair_variant<KIND, KMAJ, 256, PAIRS>(L);
-    case 224: return launch_pair_variant<KIND, KMAJ, 224, PAIRS>(L);
-    case 192: return launch_pair_variant<KIND, KMAJ, 192, PAIRS>(L);
-    case 128: return launch_pair_variant<KIND, KMAJ, 128, PAIRS>(L);
+    case 256: return launch_pair_variant<KIND, OPS, 256, PAIRS>(L);
+    case 224: return launch_pair_variant<KIND, OPS, 224, PAIRS>(L);
+    case 192: return launch_pair_variant<KIND, OPS, 192, PAIRS>(L);
+    case 128: return launch_pair_variant<KIND, OPS, 128, PAIRS>(L);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int KIND, bool KMAJ>
+template <int KIND, int OPS>
 cudaError_t launch_pair_layout(const LaunchPlan& L) {
-  if (L.pairs == 1) return launch_pair_width<KIND, KMAJ, 1>(L);
-  if (L.pairs == 2) return launch_pair_width<KIND, KMAJ, 2>(L);
+  if (L.pairs == 1) return launch_pair_width<KIND, OPS, 1>(L);
+  if (L.pairs == 2) return launch_pair_width<KIND, OPS, 2>(L);
   return cudaErrorInvalidValue;
 }
 
-template <int KIND, bool KMAJ, int PAIRS>
+template <int KIND, int OPS, int PAIRS>
 int pair_clusters_width(int bn) {
   switch (bn) {
-    case 256: return pair_clusters_variant<KIND, KMAJ, 256, PAIRS>();
-    case 224: return pair_clusters_variant<KIND, KMAJ, 224, PAIRS>();
-    case 192: return pair_clusters_variant<KIND, KMAJ, 192, PAIRS>();
-    case 128: return pair_clusters_variant<KIND, KMAJ, 128, PAIRS>();
+    case 256: return pair_clusters_variant<KIND, OPS, 256, PAIRS>();
+    case 224: return pair_clusters_variant<KIND, OPS, 224, PAIRS>();
+    case 192: return pair_clusters_variant<KIND, OPS, 192, PAIRS>();
+    case 128: return pair_clusters_variant<KIND, OPS, 128, PAIRS>();
     default: return 0;
   }
 }
 
 // Body of one gemm_<kind>_<layout>.cu: instantiates every kernel of that kind
 // and B layout (single CTA, CTA pair, two pairs; each tile width).
-#define DGT_DEFINE_VARIANTS(name, KIND, KMAJ)                                          \
-  cudaError_t launch_##name(const LaunchPlan& L) {                                     \
-    if (L.b_kmajor != (KMAJ)) return cudaErrorInvalidValue;                            \
-    return L.pair ? launch_pair_layout<KIND, KMAJ>(L) : launch_layout<KIND, KMAJ>(L);  \
-  }                                                                                    \
-  int pair_clusters_##name(int bn, int pairs) {                                        \
-    if (pairs == 1) return pair_clusters_width<KIND, KMAJ, 1>(bn);                     \
-    if (pairs == 2) return pair_clusters_width<KIND, KMAJ, 2>(bn);                     \
-    return 0;                                                                          \
+#define DGT_DEFINE_VARIANTS(name, KIND, KMAJ)                                                  \
+  cudaError_t launch_##name(const LaunchPlan& L) {                                             \
+    if (L.b_kmajor != (KMAJ) || L.swap) return cudaErrorInvalidValue;                          \
+    return L.pair ? launch_pair_layout<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN>(L)                   \
+                  : launch_layout<KIND, KMAJ>(L);                                              \
+  }                                                                                            \
+  int pair_clusters_##name(int bn, int pairs) {                                                \
+    if (pairs == 1) return pair_clusters_width<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN, 1>(bn);      \
+    if (pairs == 2) return pair_clusters_width<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN, 2>(bn);      \
+    return 0;                                                                                  \
+  }
+
+// Body of one gemm_<kind>_sw.cu: the pair kernel on the transposed product, each width.
+#define DGT_DEFINE_SWAP_VARIANTS(name, KIND)                                   \
+  cudaError_t launch_##name(const LaunchPlan& L) {                             \
+    if (L.b_kmajor || !L.pair || !L.swap || L.pairs != 1) return cudaErrorInvalidValue; \
+    return launch_pair_width<KIND, OPS_SWAP, 1>(L);                            \
   }
 
 }  // namespace dgt

@@ -421,7 +421,8 @@ def set_debug(flags: int = 0, wait_limit_ns: int = 0) -> None:
 
 
 def set_tuning(variant: int = 0, tile_n: int = 0, raster: int = 0, tail_split: int = 0) -> None:
-    """Force the kernel variant (1 single CTA, 2 CTA pair), tile width, band
+    """Force the kernel variant (1 single CTA, 2 CTA pair, 3 two pairs sharing
+    A, 4 CTA pair on the transposed product for row-major B), tile width, band
     height and tail split (1 never, 2 when possible) for later calls (0 = automatic)."""
     code = load().gemm_set_tuning(int(variant), int(tile_n), int(raster), int(tail_split))
     if code != GEMM_OK:

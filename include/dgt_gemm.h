@@ -268,7 +268,8 @@ uint64_t gemm_launch_count(void);
 /*
  * The launch plan of the calling host thread's last GEMM call that launched
  * the product kernel, as 8 integers in out[0..7]: kernel (1 single CTA, 2 CTA
- * pair, 4 two CTA pairs sharing A), tile width, band height, grid size in CTAs, K segments per tile of
+ * pair, 3 CTA pair on the transposed product C^T = B^T A^T, 4 two CTA pairs
+ * sharing A), tile width, band height, grid size in CTAs, K segments per tile of
  * the last partial round (1 = not split), tiles in flight at once, first
  * split tile, number of work items. All zero before the first such call.
  */
@@ -278,13 +279,17 @@ int gemm_last_plan(int32_t* out);
  * Tuning hook, process-wide, for subsequent calls. `variant`: 0 = chosen per
  * call, 1 = single-CTA kernel (128-row tiles), 2 = CTA-pair kernel (256-row
  * tiles), 3 = clusters of two CTA pairs that take two adjacent 256-row tiles
- * and load their shared A rows once, by TMA multicast (2 and 3 only when A
- * and B rows are 16-byte aligned or can be packed, else the single-CTA kernel
- * runs). `tile_n`: output tile width, 256, 224, 192 or 128 (0 = chosen per call).
- * `raster`: band height of the tile order in tile rows (0 = chosen per call).
- * `tail_split`: 0 or 2 = split the tiles of the last partial round along K
- * where the shape allows (the default), 1 = never split.
- * Results do not depend on any of them. Returns GEMM_ERR_INVALID_VALUE for
+ * and load their shared A rows once, by TMA multicast, 4 = CTA-pair kernel
+ * on the transposed product C^T = B^T A^T (TF32, FP16, BF16 with row-major B:
+ * 256 columns of C by `tile_n` rows per tile). 2-4 apply only when A and B
+ * rows are 16-byte aligned or can be packed, and 4 only with row-major B;
+ * otherwise the single-CTA kernel runs. `tile_n`: output tile width, 256,
+ * 224, 192 or 128 (0 = chosen per call). `raster`: band height of the tile
+ * order in tile rows (0 = chosen per call). `tail_split`: 0 or 2 = split the
+ * tiles of the last partial round along K where the shape allows (the
+ * default), 1 = never split. Results meet the same accuracy whatever the
+ * setting (their bits may differ: the order of the sum over K depends on the
+ * plan); each setting is deterministic. Returns GEMM_ERR_INVALID_VALUE for
  * values outside these sets.
  */
 int gemm_set_tuning(int variant, int tile_n, int raster, int tail_split);

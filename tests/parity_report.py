@@ -146,7 +146,8 @@ def table(rows: list[dict]) -> str:
            "|---|---|---|---|---|---|---|---|---|---|"]
     for r in rows:
         pl = r["plan"]
-        kind = {1: "single CTA", 2: "CTA pair", 4: "2 pairs sharing A"}.get(pl["kernel"], str(pl["kernel"]))
+        kind = {1: "single CTA", 2: "CTA pair", 3: "CTA pair on C^T",
+                4: "2 pairs sharing A"}.get(pl["kernel"], str(pl["kernel"]))
         plan = f"{kind}, N-tile {pl['tile_n']}, last-round K segments {pl['tail_segs']}"
         out.append(f"| {r['name']} | {r['shape']} | {'K-major' if r['layout'] else 'row-major'} | {r['how']} | "
                    f"{r['n']} | {r['n_bad']} | {r['max_e']:.2e} | {r['p99_e']:.2e} | {r.get('rule', RULE.get(r['dtype']))} | "

@@ -71,10 +71,12 @@ def _run_and_check(p, alpha, beta, use_bias, act, ldc=None, variant=0, tile_n=0)
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
 @pytest.mark.parametrize("act", ["none", "relu", "gelu", "gelu_tanh"])
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 def test_fused_epilogue_every_kernel(dtype, act, variant):
     """alpha, beta, bias and each activation on a ragged multi-tile shape, for
-    the single-CTA kernel, the CTA pair and the shared-A pair clusters."""
+    the single-CTA kernel, the CTA pair, the shared-A pair clusters and the
+    pair on the transposed product (bias along the accumulator's rows, C read
+    and written column by column)."""
     p = inputs.make_problem("epi", dtype, 300, 700, 520, seed_a=11, seed_b=12, dist_a="normal")
     _run_and_check(p, alpha=0.75, beta=-0.5, use_bias=True, act=act, variant=variant)
 
@@ -88,7 +90,7 @@ def test_fused_epilogue_terms(dtype, beta, use_bias):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "tf32"])
-@pytest.mark.parametrize("variant", [2, 3])
+@pytest.mark.parametrize("variant", [2, 3, 4])
 def test_fused_epilogue_split_tail(dtype, variant):
     """Split tiles: the epilogue applies once, to the summed segments."""
     p = inputs.make_problem("epi3", dtype, 768, 2560, 4096, seed_a=31, seed_b=32, dist_a="normal")

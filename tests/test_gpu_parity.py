@@ -17,6 +17,8 @@ from dense_gemm_tensor_gb300 import gemm, inputs
 pytestmark = pytest.mark.gpu
 
 TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "tf32": torch.float32}
+# gemm_last_plan's kernel field for each forced tuning variant
+PLAN_KERNEL = {1: 1, 2: 2, 3: 4, 4: 3}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -114,13 +116,17 @@ def test_every_tile_width_full(dtype, layout, tile_n):
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
 @pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("tile_n", [256, 224, 192, 128])
-@pytest.mark.parametrize("variant", [2, 3])
+@pytest.mark.parametrize("variant", [2, 3, 4])
 def test_pair_kernel_full(dtype, layout, tile_n, variant):
     """The CTA-pair kernel (256-row tiles over two SMs; variant 3: clusters of
-    two pairs that share A and take two adjacent tiles), forced, on shapes with
-    a ragged pair-row (M = 129: the second CTA's rows are all past M), ragged
+    two pairs that share A and take two adjacent tiles; variant 4, row-major
+    B: the transposed product, 256 columns of C by tile_n rows), forced, on
+    shapes with a ragged pair-row (M = 129: the second CTA's rows are all past
+    M; transposed: N = 300, the second tile's second CTA past N), ragged
     columns, an odd number of tile columns (the second pair's tile lies past
     N) and several waves of tiles."""
+    if variant == 4 and layout == 1:
+        pytest.skip("the transposed product is the row-major-B kernel")
     gemm.set_tuning(variant, tile_n, 2, 0)
     try:
         for (M, N, K) in [(300, 700, 520), (129, 300, 200), (1000, 1500, 336), (2048, 1024, 64)]:
@@ -130,7 +136,7 @@ def test_pair_kernel_full(dtype, layout, tile_n, variant):
             p = inputs.make_problem("pair", dtype, M, N, K, lda=-(-K // pad) * pad, ldb=ldb, layout=layout,
                                     seed_a=tile_n + M + 1, seed_b=tile_n + N + 2, dist_a="normal")
             C, Cbuf = _run(p, ldc=N + 8, fill=3.0)
-            assert gemm.last_plan()["kernel"] == 2 * (variant - 1)
+            assert gemm.last_plan()["kernel"] == PLAN_KERNEL[variant]
             _check_full(p, C)
             assert torch.all(Cbuf[:, N:] == 3.0)
     finally:
@@ -141,20 +147,22 @@ def test_pair_kernel_full(dtype, layout, tile_n, variant):
 @pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("shape", [(768, 2560, 4096), (1280, 1024, 4096), (768, 1024, 4096), (4096, 4096, 512),
                                    (768, 2816, 4096)])
-@pytest.mark.parametrize("variant", [2, 3])
+@pytest.mark.parametrize("variant", [2, 3, 4])
 def test_pair_split_tail(dtype, layout, shape, variant):
     """Tiles of the last partial round split along K (2-4 segments, chosen
     from the co-resident cluster count when each segment keeps >= 16
     k-slabs): full parity, and bitwise-equal results over repeated runs
     whatever segment arrives last."""
     M, N, K = shape
+    if variant == 4 and layout == 1:
+        pytest.skip("the transposed product is the row-major-B kernel")
     gemm.set_tuning(variant, 256, 0, 0)
     try:
         p = inputs.make_problem("split", dtype, M, N, K, layout=layout, seed_a=M + N, seed_b=K, dist_a="normal")
         C1, _ = _run(p)
         plan = gemm.last_plan()
-        assert plan["kernel"] == 2 * (variant - 1)
-        pairs = variant - 1
+        assert plan["kernel"] == PLAN_KERNEL[variant]
+        pairs = 2 if variant == 3 else 1
         tile_cols = -(-N // 256)
         tiles = -(-M // 256) * -(-tile_cols // pairs)  # work tiles: pairs adjacent 256-wide tiles each
         if K == 4096 and tiles % plan["concurrent_tiles"]:
