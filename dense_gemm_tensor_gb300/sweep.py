@@ -106,7 +106,7 @@ def markdown(recs: list[dict]) -> str:
              f"fraction {PEAK_NOTE} | torch.matmul µs |", "|---|---|---|---|---|---|---|---|---|---|---|"]
     for r in recs:
         pl = r["plan"]
-        kern = {1: "single", 2: "pair", 4: "2 pairs"}.get(pl["kernel"], str(pl["kernel"]))
+        kern = {1: "single", 2: "pair", 3: "pair on C^T", 4: "2 pairs"}.get(pl["kernel"], str(pl["kernel"]))
         lines.append(f"| {r['workload']} | {r['dtype']} | {r['M']}x{r['N']}x{r['K']} | {'K-major' if r['layout'] else 'row'} "
                      f"| {kern}, {pl['tile_n']}, {pl['tail_segs']} | {r['median_us']} | {r['mean_us']} | {r['cold_us']} "
                      f"| {r['tflops']} | {r.get('frac_of_peak', '')} | {r.get('torch_matmul_us', '')} |")
