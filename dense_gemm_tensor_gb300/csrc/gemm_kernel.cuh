@@ -518,24 +518,27 @@ __device__ __forceinline__ void epi_load_c(const GemmParams& p, uint32_t stage, 
   constexpr int ES = KIND == KIND_TF32 ? 4 : 2;
   const int l = lane & 15;
   const int col = col0 + l * (4 / ES);
-#pragma unroll 4
-  for (int rr = 0; rr < 32; rr += 2) {
-    const int r = rr + (lane >> 4);
-    const int row = row0 + r;
-    uint32_t v = 0;
+  // all 16 loads of the lane first (in flight together: the tile costs one
+  // memory latency, not one per load), then the shared-memory stores
+  uint32_t v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int row = row0 + 2 * i + (lane >> 4);
+    v[i] = 0;
     if (row < p.M && col < p.N) {
       const uint8_t* src =
           reinterpret_cast<const uint8_t*>(p.C) + (bz * p.stride_c + static_cast<long long>(row) * p.ldc + col) * ES;
       if (ES == 4 || (p.c_gran >= 4 && col + 1 < p.N)) {
-        v = *reinterpret_cast<const uint32_t*>(src);
+        v[i] = *reinterpret_cast<const uint32_t*>(src);
       } else {
-        v = reinterpret_cast<const uint16_t*>(src)[0];
-        if (col + 1 < p.N) v |= static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(src)[1]) << 16;
+        v[i] = reinterpret_cast<const uint16_t*>(src)[0];
+        if (col + 1 < p.N) v[i] |= static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(src)[1]) << 16;
       }
     }
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(epi_chunk_addr(stage, r, l >> 2) + ((l & 3) << 2)), "r"(v)
-                 : "memory");
   }
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    st_shared_u32(epi_chunk_addr(stage, 2 * i + (lane >> 4), l >> 2) + ((l & 3) << 2), v[i]);
   __syncwarp();
 }
 
@@ -562,6 +565,29 @@ __device__ __forceinline__ float epi_activation(float v, int act) {
     return 0.5f * v * (1.0f + tanhf(u));
   }
   return v;
+}
+
+// The activation applied to every element of v, the choice taken once (each
+// activation is one straight loop, so a plain epilogue runs no per-element
+// branches).
+template <int NV>
+__device__ __forceinline__ void epi_activate(float (&v)[NV], int act) {
+  switch (act) {
+    case 1:
+#pragma unroll
+      for (int k = 0; k < NV; ++k) v[k] = epi_activation(v[k], 1);
+      break;
+    case 2:
+#pragma unroll
+      for (int k = 0; k < NV; ++k) v[k] = epi_activation(v[k], 2);
+      break;
+    case 3:
+#pragma unroll
+      for (int k = 0; k < NV; ++k) v[k] = epi_activation(v[k], 3);
+      break;
+    default:
+      break;
+  }
 }
 
 // One round with the fused epilogue: out = act(alpha * acc + beta * C + bias[col]),
@@ -597,15 +623,14 @@ __device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUten
           v[k] += __half2float(bias[col0 + k]);
       }
   }
+  epi_activate(v, p.act);
   uint32_t w[16];
   if constexpr (KIND == KIND_TF32) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) w[k] = __float_as_uint(epi_activation(v[k], p.act));
+    for (int k = 0; k < 16; ++k) w[k] = __float_as_uint(v[k]);
   } else {
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-      w[k] = pack2<KIND>(__float_as_uint(epi_activation(v[2 * k], p.act)),
-                         __float_as_uint(epi_activation(v[2 * k + 1], p.act)));
+    for (int k = 0; k < 16; ++k) w[k] = pack2<KIND>(__float_as_uint(v[2 * k]), __float_as_uint(v[2 * k + 1]));
   }
   epi_put_row(stage, lane, w);
   epi_flush<KIND>(p, tmC, stage, lane, row0, col0, bz);
@@ -661,96 +686,92 @@ __device__ __forceinline__ float epi_load_elem(uint32_t addr) {
   }
 }
 
-// emit_chunk_t with the fused epilogue: each lane computes its column's 32
-// values (alpha * acc, beta * C, bias[col], activation: the order of
-// epi_round_fused) and stores them element by element.
+// Stores one staging tile of a C^T chunk (see emit_chunk_t): x[j] holds
+// C[row0 + j][col0 + lane] as fp32 bits. Neighbouring lanes trade a value so
+// that each stores whole 32-bit words, a pair of rows per step (one lane row
+// j, its partner row j + 1), 128 bytes a step for the warp, free of bank
+// conflicts. 16-bit C (one tile of 32 columns): lanes 2i and 2i+1 hold
+// columns 2i and 2i+1 and write that column pair's word in rows j and j+1
+// (rounded to the output type here). fp32 C (tile h of two, 16 columns
+// each): lanes l and l ^ 16 trade their row-(j+1) values, so in the tile of
+// the lower 16 columns lanes 0-15 write row j and lanes 16-31 row j + 1, and
+// the other way round in the upper tile.
 template <int KIND>
-__device__ __forceinline__ void emit_chunk_t_fused(const GemmParams& p, const CUtensorMap* tmC, EpiRing& ring, int lane,
-                                                int row0, int col0, int bz, const uint32_t (&r)[32]) {
-  constexpr int ES = KIND == KIND_TF32 ? 4 : 2;
-  constexpr int RC = 64 / ES;  // columns per staging tile
-  using T = typename KindTraits<KIND>::T;
-  float bias = 0.0f;
-  const bool has_bias = p.bias != nullptr && col0 + lane < p.N;
-  if (has_bias) {
-    const T b = static_cast<const T*>(p.bias)[col0 + lane];
-    if constexpr (KIND == KIND_TF32)
-      bias = b;
-    else if constexpr (KIND == KIND_BF16)
-      bias = __bfloat162float(b);
-    else
-      bias = __half2float(b);
-  }
-  for (int h = 0; h < 32 / RC; ++h) {
-    const int cb = col0 + h * RC;
-    if (cb >= p.N) break;
-    const uint32_t stage = epi_acquire(p, lane, ring);
-    if (p.beta != 0.0f) epi_load_c<KIND>(p, stage, lane, row0, cb, bz);
-    if (lane / RC == h) {
-      const int byte = (lane - h * RC) * ES;
+__device__ __forceinline__ void epi_put_cols(uint32_t stage, int lane, int h, const uint32_t (&x)[32]) {
+  if constexpr (KIND == KIND_TF32) {
+    const int k = (lane & 15) * 4;      // byte of this lane's column within a tile
+    const bool own = (lane >> 4) == h;  // this lane's column lies in tile h
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t a = epi_elem_addr(stage, j, byte);
-        float v = p.alpha * __uint_as_float(r[j]);
-        if (p.beta != 0.0f) v += p.beta * epi_load_elem<KIND>(a);
-        if (has_bias) v += bias;
-        v = epi_activation(v, p.act);
-        if constexpr (KIND == KIND_TF32)
-          st_shared_u32(a, __float_as_uint(v));
-        else
-          st_shared_u16(a, pack2<KIND>(__float_as_uint(v), 0u) & 0xFFFFu);
-      }
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x[2 * i + 1], 16);  // partner's row 2i+1
+      st_shared_u32(epi_elem_addr(stage, 2 * i + (own ? 0 : 1), k), own ? x[2 * i] : y);
     }
-    epi_flush<KIND>(p, tmC, stage, lane, row0, cb, bz);
+  } else {
+    const bool odd = lane & 1;
+    const int k = (lane >> 1) * 4;  // byte of this lane's column pair within the tile
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t t = odd ? x[2 * i] : x[2 * i + 1];
+      const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, t, 1);
+      const uint32_t w = odd ? pack2<KIND>(y, x[2 * i + 1]) : pack2<KIND>(x[2 * i], y);
+      st_shared_u32(epi_elem_addr(stage, 2 * i + (odd ? 1 : 0), k), w);
+    }
   }
 }
 
 // emit_chunk for an accumulator that holds a tile of C^T: lane l has
 // C[row0 + j][col0 + l] in r[j], j = 0..31 (32 rows of one column of C per
-// lane). Each staging tile is a 32-row box of C; neighbouring lanes trade a
-// value so that each stores whole 32-bit words, a pair of rows per step (one
-// lane row j, its partner row j + 1), 128 bytes a step for the warp, free of
-// bank conflicts. 16-bit C: lanes 2i and 2i+1 hold columns 2i and 2i+1 and
-// write the word of that column pair in rows j and j+1. fp32 C (two tiles of
-// 16 columns): lanes l and l ^ 16 trade their row-(j+1) values, so in the
-// tile of the lower 16 columns lanes 0-15 write row j and lanes 16-31 row
-// j + 1, and the other way round in the upper tile. The tile then leaves as
-// in emit_chunk. Warp-collective.
+// lane). Each staging tile is a 32-row box of C (16-bit C: one tile of 32
+// columns; fp32 C: two of 16), filled by epi_put_cols and written out as in
+// emit_chunk. With the fused epilogue each lane first computes its column's
+// values in fp32 in the order of epi_round_fused (alpha * acc, + beta * C,
+// read from the staged box of C, + bias[col], activation). Warp-collective.
 template <int KIND>
 __device__ __forceinline__ void emit_chunk_t(const GemmParams& p, const CUtensorMap* tmC, EpiRing& ring, int lane,
                                              int row0, int col0, int bz, const uint32_t (&r)[32]) {
-  if (p.fused) {
-    emit_chunk_t_fused<KIND>(p, tmC, ring, lane, row0, col0, bz, r);
-    return;
-  }
-  if constexpr (KIND == KIND_TF32) {
-    const int k = (lane & 15) * 4;  // byte of this lane's column within a tile
+  constexpr int NT = KIND == KIND_TF32 ? 2 : 1;  // staging tiles per chunk
+  constexpr int RC = 32 / NT;                    // columns per staging tile
+  constexpr int ES = KIND == KIND_TF32 ? 4 : 2;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int cb = col0 + 16 * h;
-      if (cb >= p.N) break;
-      const uint32_t stage = epi_acquire(p, lane, ring);
-      const bool own = (lane >> 4) == h;  // this lane's column lies in tile h
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, r[2 * i + 1], 16);  // partner's row 2i+1
-        st_shared_u32(epi_elem_addr(stage, 2 * i + (own ? 0 : 1), k), own ? r[2 * i] : y);
-      }
-      epi_flush<KIND>(p, tmC, stage, lane, row0, cb, bz);
-    }
-  } else {
-    if (col0 >= p.N) return;
-    const bool odd = lane & 1;
-    const int k = (lane >> 1) * 4;  // byte of this lane's column pair within the tile
+  for (int h = 0; h < NT; ++h) {
+    const int cb = col0 + h * RC;
+    if (cb >= p.N) break;
     const uint32_t stage = epi_acquire(p, lane, ring);
+    if (p.fused) {
+      using T = typename KindTraits<KIND>::T;
+      float v[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t x = odd ? r[2 * i] : r[2 * i + 1];
-      const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
-      const uint32_t w = odd ? pack2<KIND>(y, r[2 * i + 1]) : pack2<KIND>(r[2 * i], y);
-      st_shared_u32(epi_elem_addr(stage, 2 * i + (odd ? 1 : 0), k), w);
+      for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
+      if (p.beta != 0.0f) {
+        epi_load_c<KIND>(p, stage, lane, row0, cb, bz);
+        // this lane's column of the staged box (lanes of the other fp32 tile read
+        // a column of this one; their values are not stored)
+        const int byte = (lane % RC) * ES;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += p.beta * epi_load_elem<KIND>(epi_elem_addr(stage, j, byte));
+        __syncwarp();  // every lane has read the box before the tile is overwritten
+      }
+      if (p.bias != nullptr && col0 + lane < p.N) {
+        const T b = static_cast<const T*>(p.bias)[col0 + lane];
+        float bias;
+        if constexpr (KIND == KIND_TF32)
+          bias = b;
+        else if constexpr (KIND == KIND_BF16)
+          bias = __bfloat162float(b);
+        else
+          bias = __half2float(b);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += bias;
+      }
+      epi_activate(v, p.act);
+      uint32_t x[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(v[j]);
+      epi_put_cols<KIND>(stage, lane, h, x);
+    } else {
+      epi_put_cols<KIND>(stage, lane, h, r);
     }
-    epi_flush<KIND>(p, tmC, stage, lane, row0, col0, bz);
+    epi_flush<KIND>(p, tmC, stage, lane, row0, cb, bz);
   }
 }
 
