@@ -9,6 +9,11 @@
 // both CTAs' shared memory at the same offsets and leaves rows 0-127 of the
 // accumulator in the leader's tensor memory and rows 128-255 in the peer's.
 //
+// OPS (operand arrangement, see OPS_B_MN / OPS_B_K / OPS_SWAP below): with
+// OPS_SWAP the pair computes a tile of C^T = B^T A^T instead -- the rows above
+// are columns of C and the tile's BN columns are rows of C -- and the
+// epilogue transposes each accumulator chunk on its way to shared memory.
+//
 // PAIRS = 2: a cluster of four CTAs holds two pairs (ranks 0-1 and 2-3) that
 // compute two adjacent tiles of one 256-row band. CTAs of the same half (ranks
 // r and r + 2) need the same 128 rows of A, so each loads 64 of them and TMA
