@@ -356,6 +356,14 @@ constexpr double kSlabCyclesTf32Mn[4] = {564.0, 512.0, 495.0, 476.0};
 // are the plain pair's with the 256-wide penalty.
 constexpr double kSlabCyclesSwap[4] = {579.0, 493.0, 467.0, 476.0};
 constexpr double kSlabCyclesSwapTf32[4] = {576.0, 501.0, 461.0, 488.0};
+// Its epilogue (the transpose) also costs more per tile, which shows once the
+// k-loop is short: 4096 x 4096 x 1024 BF16 ran 34.4 us against 33.6 us.
+constexpr double kSwapTileCycles = 600.0;
+// The single-CTA kernel with TF32 and row-major B fetches B in eight
+// 32-column boxes per stage at width 256: at 2048^3 it ran 38.6 us where the
+// CTA pair ran 33.4 (BF16: 22.7 and 23.6 us), about 807 cycles per slab
+// against the 16-bit kernel's 672 once the fixed costs are taken out.
+constexpr double kSlabCyclesTf32MnSingle[4] = {807.0, 768.0, 726.0, 684.0};
 
 // Picks the kernel (single CTA, CTA pair, two pairs sharing A, or a CTA pair
 // on the transposed product), the tile width and the tile order.
@@ -398,10 +406,10 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
       conc = sms;
     }
     const int wi = bn == 256 ? 0 : bn == 224 ? 1 : bn == 192 ? 2 : 3;
-    const double slab = swap                                     ? (kind == KIND_TF32 ? kSlabCyclesSwapTf32[wi]
-                                                                                      : kSlabCyclesSwap[wi])
-                        : (pair && kind == KIND_TF32 && !kmajor) ? kSlabCyclesTf32Mn[wi]
-                                                                 : kSlabCycles[pair ? pairs : 0][wi];
+    const bool tf32_mn = kind == KIND_TF32 && !kmajor;
+    const double slab = swap      ? (kind == KIND_TF32 ? kSlabCyclesSwapTf32[wi] : kSlabCyclesSwap[wi])
+                        : tf32_mn ? (pair ? kSlabCyclesTf32Mn[wi] : kSlabCyclesTf32MnSingle[wi])
+                                  : kSlabCycles[pair ? pairs : 0][wi];
     const int64_t rows = pair ? 256 : 128;
     const int64_t tiles_n = (nb_ext + bn - 1) / bn;
     const int64_t tiles = nbat * ((ma + rows - 1) / rows) * ((tiles_n + pairs - 1) / pairs);
@@ -416,7 +424,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
       while (segs > 1 && kslabs / segs < kMinSegmentSlabs) --segs;
       if (segs < 1) segs = 1;
     }
-    const double tile_cost = double(kslabs) * slab + 600.0;
+    const double tile_cost = double(kslabs) * slab + 600.0 + (swap ? kSwapTileCycles : 0.0);
     // a cluster launch with pair set-up costs ~4 us more than a plain one (measured)
     double cost = double(full) * tile_cost + (pair ? kPairLaunchCycles : 0.0);
     if (rest > 0) {
