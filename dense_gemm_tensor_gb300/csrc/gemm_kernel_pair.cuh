@@ -85,7 +85,6 @@ struct PairCfg {
   static constexpr int LASTN = BNH - (NBOX - 1) * BOXN;
   static constexpr bool B_MN = OPS == OPS_B_MN;
   static constexpr int B_TX = B_MN ? (NBOX - 1) * BOX_BYTES + LASTN * BK * ES : B_BYTES;
-  static constexpr bool B_ATOM32 = MN_ATOM32 && B_MN;
   static constexpr uint32_t B_SWZ = MN_SWZ;
   static constexpr uint32_t B_SBO = MN_SBO;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
