@@ -33,7 +33,8 @@ def main():
         res = oracle.check(C.cpu().double().numpy(), ref, s, dtype or p.dtype)
         results[name] = bool(res["ok"])
 
-    cases = [("bf16", 0, 1, 256), ("bf16", 1, 2, 224), ("f16", 0, 3, 192), ("tf32", 0, 2, 256), ("tf32", 1, 1, 128)]
+    cases = [("bf16", 0, 1, 256), ("bf16", 1, 2, 224), ("f16", 0, 3, 192), ("tf32", 0, 2, 256), ("tf32", 1, 1, 128),
+             ("bf16", 0, 4, 224), ("tf32", 0, 4, 256)]
     for dtype, layout, variant, bn in cases:
         p = inputs.make_problem("chk", dtype, 700, 900, 520, layout=layout, seed_a=1, seed_b=2, dist_a="normal")
         gemm.set_tuning(variant, bn, 0, 0)
@@ -47,6 +48,15 @@ def main():
     torch.cuda.synchronize()
     results["split_segments"] = gemm.last_plan()["tail_segs"]
     check("bf16-split-gelu", p, C, alpha=0.5, act=oracle.ACT_GELU)
+    # the transposed product's split tail with the fused epilogue (beta * C read)
+    p = inputs.make_problem("chkt", "tf32", 768, 2560, 4096, seed_a=9, seed_b=10, dist_a="normal")
+    C0 = torch.ones(768, 2560, dtype=torch.float32)
+    C = C0.cuda()
+    gemm.set_tuning(4, 256, 0, 0)
+    gemm.matmul(p.a.cuda(), p.b.cuda(), C, beta=-0.5, activation="relu")
+    torch.cuda.synchronize()
+    results["swap_split_segments"] = gemm.last_plan()["tail_segs"]
+    check("tf32-swap-split-relu", p, C, beta=-0.5, c_in=C0.double().numpy(), act=oracle.ACT_RELU)
     gemm.set_tuning(0, 0, 0, 0)
     # copy-warp path (unaligned rows read in place)
     gemm.set_debug(2, 0)

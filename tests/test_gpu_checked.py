@@ -26,4 +26,5 @@ def test_checked_build_reports_no_violation():
     res = json.loads(r.stdout.strip().splitlines()[-1])
     assert res.pop("status") == 0, res
     assert res.pop("split_segments") > 1
+    assert res.pop("swap_split_segments") > 1
     assert all(res.values()), res
