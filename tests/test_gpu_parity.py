@@ -93,6 +93,26 @@ def test_small_shapes_full(dtype, layout, shape):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
+@pytest.mark.parametrize("shape", SMALL_SHAPES)
+def test_small_shapes_transposed_product(dtype, shape):
+    """The pair kernel on the transposed product (forced) on the small and
+    degenerate shapes: one element, K below one k-slab, C narrower than a
+    warp's 32 columns or than one CTA's 128, fewer rows of C than a chunk."""
+    M, N, K = shape
+    pad = 8 if dtype != "tf32" else 4
+    p = inputs.make_problem("smallt", dtype, M, N, K, seed_a=M * 3 + K, seed_b=N * 11 + K,
+                            lda=-(-K // pad) * pad, ldb=-(-N // pad) * pad, dist_a="normal")
+    gemm.set_tuning(4, 0, 0, 0)
+    try:
+        C, Cbuf = _run(p, ldc=N + 8, fill=3.0)
+        assert gemm.last_plan()["kernel"] == PLAN_KERNEL[4]
+    finally:
+        gemm.set_tuning(0, 0, 0, 0)
+    _check_full(p, C)
+    assert torch.all(Cbuf[:, N:] == 3.0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
 @pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("tile_n", [256, 224, 192, 128])
 def test_every_tile_width_full(dtype, layout, tile_n):
