@@ -79,3 +79,20 @@ def test_bench_rejects_short_warmup():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2", "--impl", "reference"],
                        capture_output=True, text=True, timeout=120)
     assert r.returncode != 0
+
+
+def test_kernel_names_and_traffic_record():
+    """The launch plan -> kernel name mapping (as ncu names the kernels) for
+    every plan kind, and the committed traffic record: it names the kernels of
+    the plans it was captured with and carries the device sources' hash."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.kernel_name("bf16", {"kernel": 1, "tile_n": 256}) == "gemm_kernel<1, 0, 256>"
+    assert bench.kernel_name("tf32", {"kernel": 2, "tile_n": 224}) == "gemm_kernel_pair<2, 0, 224, 1>"
+    assert bench.kernel_name("f16", {"kernel": 3, "tile_n": 224}) == "gemm_kernel_pair<0, 2, 224, 1>"
+    assert bench.kernel_name("bf16", {"kernel": 4, "tile_n": 256}) == "gemm_kernel_pair<1, 0, 256, 2>"
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    for dt in ("tf32", "f16", "bf16"):
+        assert rec[dt]["kernel"].startswith("gemm_kernel") and rec[dt]["bytes"] > 0
+    assert len(rec["kernel_sources_sha256"]) == 64
