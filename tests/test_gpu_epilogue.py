@@ -132,6 +132,26 @@ def test_k_zero_with_epilogue(dtype):
     assert oracle.check(C.cpu().double().numpy(), ref, s, dtype)["ok"]
 
 
+@pytest.mark.parametrize("act", ["gelu", "gelu_tanh"])
+def test_gelu_precision_dense_grid(act):
+    """Both GELU forms on 65536 points of [-12, 12] and at large |x| (where they
+    saturate), through the K = 0 product with beta = 1 (C = act(C), fp32 C):
+    within 2e-6 * |x| of the float64 oracle, far inside the epilogue's
+    acceptance bound."""
+    M, N = 64, 1024
+    x = np.linspace(-12.0, 12.0, M * N).astype(np.float32)
+    x[:8] = [-1000.0, -50.0, -1e-20, 0.0, 1e-20, 50.0, 1000.0, -0.0]
+    C = torch.from_numpy(x.reshape(M, N).copy()).cuda()
+    A = torch.empty((M, 0), dtype=torch.float32, device="cuda")
+    B = torch.empty((0, N), dtype=torch.float32, device="cuda")
+    gemm.matmul(A, B, C, beta=1.0, activation=act)
+    torch.cuda.synchronize()
+    xd = x.astype(np.float64)
+    ref = oracle.gelu(xd) if act == "gelu" else oracle.gelu_tanh(xd)
+    err = np.abs(C.cpu().double().numpy().ravel() - ref)
+    assert np.all(err <= 2e-6 * np.abs(xd)), (act, float(np.max(err / np.maximum(np.abs(xd), 1e-30))))
+
+
 def test_epilogue_argument_errors():
     A = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
     C = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
