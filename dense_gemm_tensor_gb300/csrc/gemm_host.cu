@@ -365,6 +365,31 @@ constexpr double kSwapTileCycles = 600.0;
 // against the 16-bit kernel's 672 once the fixed costs are taken out.
 constexpr double kSlabCyclesTf32MnSingle[4] = {807.0, 768.0, 726.0, 684.0};
 
+// Cycles per k-slab of a tile for a kernel family and tile width (wi: index
+// into kTileWidths / kPairTileWidths).
+double slab_cycles(int kind, bool kmajor, bool pair, int pairs, bool swap, int wi) {
+  if (swap) return kind == KIND_TF32 ? kSlabCyclesSwapTf32[wi] : kSlabCyclesSwap[wi];
+  if (kind == KIND_TF32 && !kmajor) return pair ? kSlabCyclesTf32Mn[wi] : kSlabCyclesTf32MnSingle[wi];
+  return kSlabCycles[pair ? pairs : 0][wi];
+}
+
+// Band height of the tile order, in tile rows of `rows` rows each (before
+// clamping to the tile rows there are). `nb_ext`: the extent of the other side
+// of the tile grid (N, or M for the transposed product).
+int band_rows(bool pair, bool swap, int64_t K, int64_t nb_ext, int es, int64_t rows) {
+  // the transposed product: bands 16 tile rows high (at 4096^3 that is every
+  // 256-column block of C, so consecutive tiles share one block of A's rows)
+  // ran about 1.7% faster than 2 (16-bit) or 9 (TF32)
+  if (swap) return 16;
+  // 2 pair rows / 8 single-CTA rows (measured best at 4096^3) while B stays
+  // resident in L2; for a larger B, which is re-read once per band, as many
+  // rows as keep the band's A rows within ~40 MB of L2
+  const int band_min = pair ? 2 : 8;
+  if (double(K) * double(nb_ext) * es <= 64.0e6) return band_min;
+  const int band = int(40.0e6 / (double(rows) * double(K) * es));
+  return band < band_min ? band_min : band > 16 ? 16 : band;
+}
+
 // Picks the kernel (single CTA, CTA pair, two pairs sharing A, or a CTA pair
 // on the transposed product), the tile width and the tile order.
 //
@@ -406,10 +431,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
       conc = sms;
     }
     const int wi = bn == 256 ? 0 : bn == 224 ? 1 : bn == 192 ? 2 : 3;
-    const bool tf32_mn = kind == KIND_TF32 && !kmajor;
-    const double slab = swap      ? (kind == KIND_TF32 ? kSlabCyclesSwapTf32[wi] : kSlabCyclesSwap[wi])
-                        : tf32_mn ? (pair ? kSlabCyclesTf32Mn[wi] : kSlabCyclesTf32MnSingle[wi])
-                                  : kSlabCycles[pair ? pairs : 0][wi];
+    const double slab = slab_cycles(kind, kmajor, pair, pairs, swap, wi);
     const int64_t rows = pair ? 256 : 128;
     const int64_t tiles_n = (nb_ext + bn - 1) / bn;
     const int64_t tiles = nbat * ((ma + rows - 1) / rows) * ((tiles_n + pairs - 1) / pairs);
@@ -439,20 +461,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
       const int64_t tiles_m = (ma + rows - 1) / rows;
       const int64_t work = tiles + (segs - 1) * rest;
       const int64_t grid_tiles = work < conc ? work : conc;
-      // band height: 2 pair rows / 8 single-CTA rows (measured best at 4096^3) while
-      // B stays resident in L2; for a larger B, which is re-read once per band,
-      // as many rows as keep the band's A rows within ~40 MB of L2
-      const int band_min = pair ? 2 : 8;
-      int band = band_min;
-      if (double(K) * double(nb_ext) * es > 64.0e6) {
-        band = int(40.0e6 / (double(rows) * double(K) * es));
-        if (band < band_min) band = band_min;
-        if (band > 16) band = 16;
-      }
-      // the transposed product: bands 16 tile rows high (at 4096^3 that is every
-      // 256-column block of C, so consecutive tiles share one block of A's rows)
-      // ran about 1.7% faster than 2 (16-bit) or 9 (TF32)
-      if (swap) band = 16;
+      const int band = band_rows(pair, swap, K, nb_ext, es, rows);
       best = TilePlan{pair, pairs, bn, int(tiles_m < band ? tiles_m : band),
                       int(pair ? 2 * pairs * grid_tiles : grid_tiles), segs, conc, swap};
     }
