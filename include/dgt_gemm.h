@@ -240,7 +240,10 @@ const char* gemm_status_string(int status);
  * *out: 0 when no kernel gave up waiting since the last reset, else a nonzero
  * code (bits 0-3 kind: 1 = wait time limit exceeded; bits 4-7 role: 1 TMA
  * producer, 2 MMA issuer, 3 epilogue, 4 copy warps, 5 teardown; bits 8-15
- * pipeline stage; bits 16-31 CTA index). Returns GEMM_OK, or
+ * pipeline stage; bits 16-31 CTA index. In a library built with range checks
+ * (the build's `checked` option, a test configuration) kind 3 = an access
+ * outside its shared-memory, tensor-memory or scratch range was skipped, with
+ * the check site in bits 4-11). Returns GEMM_OK, or
  * GEMM_ERR_DEVICE_TIMEOUT when *out is nonzero, or GEMM_ERR_LAUNCH when the
  * synchronisation failed. The word is sticky until gemm_reset_device_status.
  */
