@@ -401,8 +401,11 @@ int band_rows(bool pair, bool swap, int64_t K, int64_t nb_ext, int es, int64_t r
 // the transposed product unless forced: its epilogue is the costlier one there
 // (4096^3 with beta * C: 100.2 against 97.4 us for BF16, 181.8 against
 // 176.8 us for TF32).
+//
+// pair_conc / quad_conc > 0 give the co-resident CTA pairs / clusters of two
+// pairs instead of the occupancy query (gemm_plan_query, without a device).
 TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es, bool kmajor, bool all_tma,
-                     int sms, int64_t nbat, bool fused) {
+                     int sms, int64_t nbat, bool fused, int pair_conc = 0, int quad_conc = 0) {
   const int64_t kslabs = (K * es + 127) / 128;
   const int fv = g_force_variant.load(std::memory_order_relaxed);
   const int fb = g_force_bn.load(std::memory_order_relaxed);
@@ -425,7 +428,8 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
     int conc;  // work tiles in flight
     if (pair) {
       // (the transposed product's kernel has the same cluster shape and one CTA per SM)
-      conc = pair_clusters(dev, kind, kmajor, bn, pairs);
+      const int given = pairs == 1 ? pair_conc : quad_conc;
+      conc = given > 0 ? given : pair_clusters(dev, kind, kmajor, bn, pairs);
       if (conc <= 0) return;
     } else {
       conc = sms;
@@ -1073,6 +1077,22 @@ int gemm_free_workspaces(void) {
 int gemm_last_plan(int32_t* out) {
   if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
   memcpy(out, dgt::t_last_plan, sizeof(dgt::t_last_plan));
+  return GEMM_OK;
+}
+
+int gemm_plan_query(int kind, int64_t M, int64_t N, int64_t K, int layout, int64_t batch, int fused, int sms,
+                    int pair_clusters, int quad_clusters, int32_t* out) {
+  if (out == nullptr || kind < dgt::KIND_F16 || kind > dgt::KIND_E5M2 || M < 1 || N < 1 || K < 1 || batch < 1 ||
+      (layout != GEMM_B_ROW_MAJOR && layout != GEMM_B_K_MAJOR) || sms < 2 || pair_clusters < 1 || quad_clusters < 1)
+    return GEMM_ERR_INVALID_VALUE;
+  const bool fp8 = kind == dgt::KIND_E4M3 || kind == dgt::KIND_E5M2;
+  const int es = kind == dgt::KIND_TF32 ? 4 : fp8 ? 1 : 2;
+  const bool kmajor = layout == GEMM_B_K_MAJOR || fp8;  // a row-major FP8 B is transposed first
+  const dgt::TilePlan plan = dgt::choose_plan(-1, kind, M, N, K, es, kmajor, true, sms, batch, fused != 0,
+                                              pair_clusters, quad_clusters);
+  const int32_t info[6] = {plan.swap ? 3 : plan.pair ? 2 * plan.pairs : 1, plan.bn, plan.raster, plan.grid,
+                           plan.segs, plan.conc};
+  memcpy(out, info, sizeof(info));
   return GEMM_OK;
 }
 

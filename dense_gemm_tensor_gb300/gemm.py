@@ -49,7 +49,8 @@ EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_tf32_ex", "gemm_f16_ex", 
            "gemm_status_string", "gemm_get_device_status", "gemm_reset_device_status", "gemm_set_debug",
            "gemm_launch_count", "gemm_set_tuning", "gemm_last_plan", "gemm_free_workspaces",
            "gemm_bf16_static_scratch", "gemm_tf32_strided_batched", "gemm_f16_strided_batched",
-           "gemm_bf16_strided_batched", "gemm_e4m3_strided_batched", "gemm_e5m2_strided_batched")
+           "gemm_bf16_strided_batched", "gemm_e4m3_strided_batched", "gemm_e5m2_strided_batched",
+           "gemm_plan_query")
 
 _lib = None
 
@@ -100,6 +101,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.gemm_last_plan.restype = ctypes.c_int
     lib.gemm_free_workspaces.argtypes = []
     lib.gemm_free_workspaces.restype = ctypes.c_int
+    ci = ctypes.c_int
+    lib.gemm_plan_query.argtypes = [ci, i64, i64, i64, ci, i64, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_int32)]
+    lib.gemm_plan_query.restype = ci
     _lib = lib
     return lib
 
@@ -430,6 +434,21 @@ def set_tuning(variant: int = 0, tile_n: int = 0, raster: int = 0, tail_split: i
 
 
 PLAN_FIELDS = ("kernel", "tile_n", "raster", "grid", "tail_segs", "concurrent_tiles", "tail_start", "work_items")
+
+
+_KIND_CODE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4}
+
+
+def plan_query(dtype: str, M: int, N: int, K: int, *, layout: int = GEMM_B_ROW_MAJOR, batch: int = 1,
+               fused: bool = False, sms: int = 152, pair_clusters: int = 76, quad_clusters: int = 36) -> dict:
+    """The plan the library's cost model picks for a product, without a device
+    (gemm_plan_query; defaults: a GB300's SM and cluster counts)."""
+    buf = (ctypes.c_int32 * 6)()
+    code = load().gemm_plan_query(_KIND_CODE[dtype], M, N, K, layout, batch, int(fused), sms, pair_clusters,
+                                  quad_clusters, buf)
+    if code != GEMM_OK:
+        raise GemmError(code, "gemm_plan_query")
+    return dict(zip(PLAN_FIELDS[:6], list(buf)))
 
 
 def last_plan() -> dict:

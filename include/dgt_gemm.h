@@ -297,6 +297,21 @@ int gemm_last_plan(int32_t* out);
  */
 int gemm_set_tuning(int variant, int tile_n, int raster, int tail_split);
 
+/*
+ * Test hook, needs no device: the plan the cost model chooses for one product
+ * (or a strided batch of `batch`) of kind `kind` -- 0 FP16, 1 BF16, 2 TF32,
+ * 3 E4M3, 4 E5M2 -- with M, N, K, B `layout`, and `fused` != 0 for a call with
+ * a fused epilogue, on a device with `sms` SMs that holds `pair_clusters` CTA
+ * pairs and `quad_clusters` clusters of two pairs at once (GB300: 152, 76,
+ * 36), assuming 16-byte-aligned operands. out[0..5] = kernel, tile width,
+ * band height, grid size in CTAs, K segments per tile of the last partial
+ * round, tiles in flight (as gemm_last_plan; before any limit of the split-tail
+ * scratch). The tuning hook's settings apply. Returns GEMM_ERR_INVALID_VALUE
+ * for out-of-range arguments.
+ */
+int gemm_plan_query(int kind, int64_t M, int64_t N, int64_t K, int layout, int64_t batch, int fused, int sms,
+                    int pair_clusters, int quad_clusters, int32_t* out);
+
 #ifdef __cplusplus
 }
 #endif
