@@ -392,3 +392,22 @@ def test_fp16_overflow_is_ieee_infinity():
     assert torch.all(C[:, 0] == 4096.0)
     assert torch.all(C[:, 1] == float("inf")) and torch.all(C[:, 2] == float("-inf"))
     assert torch.all(C[:, 3] == 65504.0)
+
+
+@pytest.mark.parametrize("dtype,shape,layout", [
+    ("bf16", (4096, 4096, 4096), 0), ("tf32", (4096, 4096, 4096), 0), ("f16", (4096, 4096, 4096), 1),
+    ("bf16", (8192, 8192, 2048), 0), ("bf16", (2048, 2048, 2048), 0), ("tf32", (2048, 2048, 2048), 0),
+    ("bf16", (6144, 6144, 512), 0), ("tf32", (1024, 8192, 4096), 1), ("bf16", (768, 2560, 4096), 0),
+])
+def test_plan_query_matches_the_launched_plan(dtype, shape, layout):
+    """gemm_plan_query (the cost model without a device, given this GPU's SM
+    count) names the plan that the call then launches on a GB300."""
+    props = torch.cuda.get_device_properties(0)
+    if props.multi_processor_count != 152:
+        pytest.skip("the plan query's cluster counts are those of a 152-SM GB300")
+    M, N, K = shape
+    p = inputs.make_problem("planq", dtype, M, N, K, layout=layout, seed_a=3, seed_b=4)
+    _run(p)
+    launched = gemm.last_plan()
+    predicted = gemm.plan_query(dtype, M, N, K, layout=layout, sms=props.multi_processor_count)
+    assert {k: launched[k] for k in predicted} == predicted
