@@ -70,7 +70,9 @@ def test_threads_with_their_own_streams():
 def test_cuda_graph_capture_and_replay():
     probs = [inputs.make_problem("g0", "bf16", 768, 2560, 4096, seed_a=31, seed_b=32, dist_a="normal"),
              inputs.make_problem("g1", "tf32", 1000, 900, 700, seed_a=33, seed_b=34),
-             inputs.make_problem("g2", "f16", 300, 520, 200, layout=1, seed_a=35, seed_b=36)]
+             inputs.make_problem("g2", "f16", 300, 520, 200, layout=1, seed_a=35, seed_b=36),
+             # the pair on the transposed product with a split tail (row-major B)
+             inputs.make_problem("g3", "bf16", 1280, 1024, 4096, seed_a=37, seed_b=38, dist_a="normal")]
     s = torch.cuda.Stream()
     dev = [(p.a.cuda(), p.b.cuda(), torch.empty((p.M, p.N), dtype=TORCH[p.dtype], device="cuda")) for p in probs]
     with torch.cuda.stream(s):  # first calls outside capture: the stream's scratch is allocated here
