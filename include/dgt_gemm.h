@@ -24,8 +24,9 @@
  *   gemm_f16 / gemm_bf16: IEEE binary16 / bfloat16 operands (passed as their
  *              16-bit patterns); fp32 accumulation; C rounded to the input
  *              type with round-to-nearest-even (IEEE overflow to +-inf).
- *   The order of the fp32 additions is unspecified; results are deterministic
- *   run to run (no atomics).
+ *   The order of the fp32 additions is unspecified (it depends on the launch
+ *   plan); results are deterministic run to run (no value is added
+ *   atomically: split tiles add their partial sums in a fixed order).
  *
  * Ownership and memory: every pointer is device memory (or managed memory) of
  * the current CUDA device, owned by the caller. C is fully overwritten and
