@@ -10,6 +10,7 @@
 // array in this library's device memory instead.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -24,38 +25,42 @@ constexpr size_t kStaticScratchBytes = dgt::kSplitCounterBytes + (size_t(16) << 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 struct StaticScratch {
-  int status;  // GEMM_OK once set up on that device
-  void* ptr;   // device address of g_static_scratch on that device
+  std::atomic<bool> ready{false};  // set up on that device
+  void* ptr = nullptr;             // device address of g_static_scratch on that device
 };
 StaticScratch g_scratch[64];
-std::once_flag g_scratch_once[64];
+std::mutex g_scratch_mutex;
 
 // Per device, on the first call with that device current: look up the
 // array's device address (the name is only a host-side stand-in) and zero
-// the counters. Allocates nothing.
+// the counters. Allocates nothing. A set-up that fails (for instance one
+// attempted inside a stream capture, where the synchronisation is not
+// allowed) leaves the device not set up, so the next call tries again.
 int static_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
     return GEMM_ERR_UNSUPPORTED_DEVICE;
   }
-  std::call_once(g_scratch_once[dev], [dev] {
-    StaticScratch& s = g_scratch[dev];
-    s.status = GEMM_ERR_LAUNCH;
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
-      cudaGetLastError();
-      return;
+  StaticScratch& s = g_scratch[dev];
+  if (!s.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!s.ready.load(std::memory_order_relaxed)) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+      }
+      if (cudaMemset(p, 0, dgt::kSplitCounterBytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+      }
+      s.ptr = p;
+      s.ready.store(true, std::memory_order_release);
     }
-    if (cudaMemset(p, 0, dgt::kSplitCounterBytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
-      cudaGetLastError();
-      return;
-    }
-    s.ptr = p;
-    s.status = GEMM_OK;
-  });
-  *out = g_scratch[dev].ptr;
-  return g_scratch[dev].status;
+  }
+  *out = s.ptr;
+  return GEMM_OK;
 }
 
 }  // namespace

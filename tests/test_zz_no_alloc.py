@@ -4,15 +4,17 @@ Such callers (a serving process whose memory pool owns the whole device, a
 plug-in that must not allocate behind its host, a latency-bound path that
 cannot absorb a cudaFree) get the same kernels as gemm_bf16 with the
 split-tile scratch taken from the library's fixed 16 MiB device array. These
-checks call it through the C interface and compare it with gemm_bf16, within
-the acceptance tolerance the parity tests use, on two calls in a row.
+checks call it through the C interface, twice in a row per shape, and hold
+each result to the float64 oracle with the acceptance rule of the parity
+tests. The shapes whose plan splits its last round of tiles along K are
+asserted to split, so their fp32 partial tiles provably pass through the
+fixed array.
 
 This file is collected last so that, if it fails, a run stopped at the first
 failure has already run every other test; it also passes on its own in a
 fresh process.
 """
 
-import numpy as np
 import pytest
 import torch
 
@@ -21,8 +23,17 @@ from dense_gemm_tensor_gb300 import gemm, inputs
 
 pytestmark = pytest.mark.gpu
 
-SCRATCH_BYTES = 16 << 20          # fp32 partial tiles the fixed array holds
-ITEM_BYTES = 2 * 128 * 256 * 4    # one split work item: both CTAs' 128 x 256 fp32 partials
+SCRATCH_BYTES = 16 << 20  # fp32 partial tiles the fixed array holds
+
+
+def split_bytes(plan: dict) -> int:
+    """Scratch the plan's split tail needs: every split work item holds one
+    128 x tile_n fp32 partial per CTA of its cluster (four CTAs for the
+    two-pair kernel, two otherwise)."""
+    if plan["tail_segs"] <= 1:
+        return 0
+    ctas = 4 if plan["kernel"] == 4 else 2
+    return (plan["work_items"] - plan["tail_start"]) * ctas * 128 * plan["tile_n"] * 4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -39,60 +50,64 @@ def _lib():
     assert gemm.device_status() == 0
 
 
-def _pointers(p):
-    A = p.a.cuda()
-    B = p.b.cuda()
-    return A, B
-
-
-@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (768, 2560, 4096), (300, 520, 200)])
-def test_matches_gemm_bf16_on_two_calls(shape):
-    M, N, K = shape
-    p = inputs.make_problem("noalloc", "bf16", M, N, K, dist_a="normal", dist_b="normal", seed_a=M + 3, seed_b=N + 5)
-    A, B = _pointers(p)
-    ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    code = gemm.gemm_bf16(M, N, K, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, ref.data_ptr(), N, 0, None)
+def _reference_plan(p):
+    """gemm_bf16's plan for the problem (the static call must launch the same)."""
+    A, B = p.a.cuda(), p.b.cuda()
+    C = torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda")
+    code = gemm.gemm_bf16(p.M, p.N, p.K, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, C.data_ptr(), p.N, 0, None)
     assert code == gemm.GEMM_OK
     torch.cuda.synchronize()
-    plan = gemm.last_plan()
+    return gemm.last_plan(), A, B
+
+
+# (M, N, K, splits): the two split shapes take the CTA pair on the transposed
+# product (three K segments per split tile, 13.8 MB of partials) and the plain
+# CTA pair (two segments, 16.5 MB: just inside the array); the others split nothing.
+SHAPES = [(1792, 3072, 4096, True), (2048, 3072, 4096, True), (4096, 4096, 4096, False), (300, 520, 200, False)]
+
+
+@pytest.mark.parametrize("M,N,K,splits", SHAPES)
+def test_matches_oracle_on_two_calls(M, N, K, splits):
+    p = inputs.make_problem("noalloc", "bf16", M, N, K, dist_a="normal", dist_b="normal", seed_a=M + 3, seed_b=N + 5)
+    plan, A, B = _reference_plan(p)
+    need = split_bytes(plan)
+    if splits:
+        assert plan["tail_segs"] > 1, plan
+        assert 0 < need <= SCRATCH_BYTES, (need, plan)
+    else:
+        assert need == 0, plan
+    c_ref = oracle.gemm(M, N, K, p.a, p.lda, p.b, p.ldb, 0)
     s = oracle.abs_gemm(M, N, K, p.a, p.lda, p.b, p.ldb, 0)
-    want = ref.cpu().double().numpy()
+    first = None
     for call in range(2):
         out = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
         code = gemm.gemm_bf16_static_scratch(M, N, K, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, out.data_ptr(), N,
                                              0, None)
         assert code == gemm.GEMM_OK, gemm.status_string(code)
         torch.cuda.synchronize()
-        assert gemm.last_plan() == plan            # the same kernels and split as gemm_bf16
-        got = out.cpu().double().numpy()
-        diff = np.abs(got - want)
-        assert np.all(diff <= oracle.allowed_error(want, s, "bf16")), f"call {call}: max diff {diff.max()}"
+        assert gemm.last_plan() == plan  # the same kernels and split as gemm_bf16
+        res = oracle.check(out.cpu().double().numpy(), c_ref, s, "bf16")
+        assert res["ok"], f"call {call}: {res}"
+        if first is None:
+            first = out.clone()
+        else:
+            assert torch.equal(out, first)  # the second call over the same array gives the same bits
     assert gemm.device_status() == 0
 
 
-def test_split_shape_uses_the_fixed_scratch_and_big_needs_are_refused():
-    """A shape whose last round splits runs inside the 16 MiB; a plan needing
-    more is refused with GEMM_ERR_SCRATCH_LIMIT and launches nothing."""
-    # 1536 x 4864: 114 tiles of 256 x 256; with 76 co-resident pairs the last
-    # round's 38 tiles split in two along K -> 76 items of 256 KiB = 19 MiB
-    M, N, K = 1536, 4864, 4096
+def test_plan_beyond_the_array_is_refused():
+    """A plan whose split partials exceed the 16 MiB is refused with
+    GEMM_ERR_SCRATCH_LIMIT before anything is launched."""
+    M, N, K = 2560, 2560, 4096  # CTA pair, 256-wide tiles, three segments: 18 MiB of partials
     p = inputs.make_problem("noalloc_big", "bf16", M, N, K, seed_a=11, seed_b=12)
-    A, B = _pointers(p)
-    ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    assert gemm.gemm_bf16(M, N, K, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, ref.data_ptr(), N, 0, None) == 0
-    torch.cuda.synchronize()
-    plan = gemm.last_plan()
-    need = (plan["work_items"] - plan["tail_start"]) * ITEM_BYTES if plan["tail_segs"] > 1 else 0
+    plan, A, B = _reference_plan(p)
+    assert split_bytes(plan) > SCRATCH_BYTES, plan
     out = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
     launches = gemm.launch_count()
     code = gemm.gemm_bf16_static_scratch(M, N, K, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, out.data_ptr(), N, 0,
                                          None)
     torch.cuda.synchronize()
-    if need > SCRATCH_BYTES:
-        assert code == gemm.GEMM_ERR_SCRATCH_LIMIT
-        assert gemm.launch_count() == launches
-        assert torch.all(out == 7.0)
-        assert "scratch" in gemm.status_string(code)
-    else:
-        assert code == gemm.GEMM_OK
-        assert torch.equal(out, ref)
+    assert code == gemm.GEMM_ERR_SCRATCH_LIMIT
+    assert gemm.launch_count() == launches
+    assert torch.all(out == 7.0)
+    assert "scratch" in gemm.status_string(code)
