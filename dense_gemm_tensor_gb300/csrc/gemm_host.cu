@@ -113,7 +113,11 @@ __global__ void __launch_bounds__(256) transpose_bytes_kernel(const uint8_t* __r
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s
+// Default bound of every wait inside the kernels: far above any wait of a
+// launch that makes progress (a 16384^3 product takes a few milliseconds), so
+// that a launch slowed by other work sharing the GPU does not give up and
+// leave C unspecified, yet a launch that can never finish still ends.
+constexpr uint64_t kDefaultWaitLimitNs = 10000000000ull;  // 10 s
 
 struct DeviceInfo {
   int status;  // GEMM_OK or the reason this device cannot run the kernels
@@ -150,8 +154,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 // Looks up (once per device) whether the current device is an sm_103 part,
-// its SM count and the device address of the status words.
-int current_device(const DeviceInfo** out) {
+// its SM count and the device address of the status words; `dev_out` (if
+// given) receives the device's ordinal.
+int current_device(const DeviceInfo** out, int* dev_out = nullptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -178,11 +183,12 @@ int current_device(const DeviceInfo** out) {
     d.status = GEMM_OK;
   });
   *out = &g_dev[dev];
+  if (dev_out != nullptr) *dev_out = dev;
   return g_dev[dev].status;
 }
 
-// Device (or managed) memory of the current device?
-bool is_device_memory(const void* ptr) {
+// Device (or managed) memory of device `dev` (the current one)?
+bool is_device_memory(const void* ptr, int dev) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
     cudaGetLastError();
@@ -190,8 +196,6 @@ bool is_device_memory(const void* ptr) {
   }
   if (a.type == cudaMemoryTypeManaged) return true;
   if (a.type != cudaMemoryTypeDevice) return false;
-  int dev = -1;
-  cudaGetDevice(&dev);
   return a.device == dev;
 }
 
@@ -212,23 +216,75 @@ int granularity(const void* p, int64_t ld, int es) {
   return g;
 }
 
+// A few entries of host-side work per calling thread, keyed by the plain
+// numbers it was computed from (no device state enters it), so an entry can
+// never go stale: the same key always yields the same value. Calls that repeat
+// a shape on the same buffers -- the common case in a loop -- skip the work.
+template <int NK, class Val, int N>
+struct TinyCache {
+  uint64_t keys[N][NK];
+  Val vals[N];
+  bool used[N] = {};
+  int next = 0;
+  const Val* find(const uint64_t (&k)[NK]) const {
+    for (int i = 0; i < N; ++i)
+      if (used[i] && memcmp(keys[i], k, sizeof(k)) == 0) return &vals[i];
+    return nullptr;
+  }
+  void put(const uint64_t (&k)[NK], const Val& v) {
+    memcpy(keys[next], k, sizeof(k));
+    vals[next] = v;
+    used[next] = true;
+    next = (next + 1) % N;
+  }
+};
+
 // 3-D tiled tensor map: x innermost (contiguous), y rows `row_bytes` apart, z
 // matrices of a batch `mat_bytes` apart (depth 1 for one product, whose z is
-// always 0). Boxes are box_inner x box_outer x 1.
+// always 0). Boxes are box_inner x box_outer x 1. Encoded maps are cached per
+// thread (a map is a pure function of these arguments).
 bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint64_t depth, uint64_t mat_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encoder();
-  if (!fn) return false;
+  thread_local TinyCache<9, CUtensorMap, 16> cache;
   if (depth == 1) mat_bytes = row_bytes * outer;  // never stepped; a stride that spans the matrix
   if (mat_bytes == 0 || mat_bytes % 16 != 0 || mat_bytes >= (uint64_t(1) << 40)) return false;
+  const uint64_t key[9] = {uint64_t(dt), uint64_t(reinterpret_cast<uintptr_t>(base)), inner, outer, row_bytes,
+                           depth, mat_bytes, (uint64_t(box_inner) << 32) | box_outer, uint64_t(swizzle)};
+  if (const CUtensorMap* hit = cache.find(key)) {
+    *m = *hit;
+    return true;
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encoder();
+  if (!fn) return false;
   cuuint64_t dims[3] = {inner, outer, depth};
   cuuint64_t strides[2] = {row_bytes, mat_bytes};
   cuuint32_t box[3] = {box_inner, box_outer, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache.put(key, *m);
+  return true;
+}
+
+// The kernel of two CTA pairs sharing A loads it with a cluster-multicast TMA
+// copy. The library runs it only in a process that sees exactly one CUDA
+// device (and never in a build with DGT_NO_MULTICAST): every multicast copy
+// then reads the memory of the one GPU in use. `dev` < 0 (a plan query
+// without a device) asks about such a one-GPU process.
+bool multicast_allowed(int dev) {
+  if (DGT_NO_MULTICAST) return false;
+  if (dev < 0) return true;
+  static const bool one_device = [] {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    return n == 1;
+  }();
+  return one_device;
 }
 
 // Co-resident CTA pairs of each pair-kernel variant, per device (-1 = not queried yet).
@@ -404,12 +460,10 @@ int band_rows(bool pair, bool swap, int64_t K, int64_t nb_ext, int es, int64_t r
 //
 // pair_conc / quad_conc > 0 give the co-resident CTA pairs / clusters of two
 // pairs instead of the occupancy query (gemm_plan_query, without a device).
-TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es, bool kmajor, bool all_tma,
-                     int sms, int64_t nbat, bool fused, int pair_conc = 0, int quad_conc = 0) {
+TilePlan choose_plan_uncached(int dev, int kind, int64_t M, int64_t N, int64_t K, int es, bool kmajor, bool all_tma,
+                              int sms, int64_t nbat, bool fused, int pair_conc, int quad_conc, int fv, int fb, int fr,
+                              int fs) {
   const int64_t kslabs = (K * es + 127) / 128;
-  const int fv = g_force_variant.load(std::memory_order_relaxed);
-  const int fb = g_force_bn.load(std::memory_order_relaxed);
-  const int fr = g_force_raster.load(std::memory_order_relaxed);
   TilePlan best{false, 1, 256, 8, sms, 1, sms, false};
   double best_cost = -1.0;
   // the transposed product: C's columns take the 256-row side of the pair's tile
@@ -423,6 +477,7 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
     if (pair && !all_tma) return;
     if (swap && !(swap_ok && pair && pairs == 1)) return;
     if (swap && fused && fv != 4) return;
+    if (pairs == 2 && !multicast_allowed(dev)) return;
     // extents of the tile grid: the MMA's A side (256-row pair tiles) and its B side (bn wide)
     const int64_t ma = swap ? N : M, nb_ext = swap ? M : N;
     int conc;  // work tiles in flight
@@ -442,7 +497,6 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
     const int64_t full = tiles / conc, rest = tiles % conc;
     // pair kernel: the tiles of the last partial round may be split along K
     // into `segs` pieces run by different pairs (fp32 partials summed at the end)
-    const int fs = g_force_split.load(std::memory_order_relaxed);
     int segs = 1;
     if (pair && rest > 0 && fs != 1) {
       segs = int(conc / rest);
@@ -480,6 +534,28 @@ TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es,
   }
   if (fr) best.raster = fr;
   return best;
+}
+
+// choose_plan_uncached with the tuning hook's settings, cached per thread (the
+// plan is a pure function of the shape, the device's SM and cluster counts and
+// those settings).
+TilePlan choose_plan(int dev, int kind, int64_t M, int64_t N, int64_t K, int es, bool kmajor, bool all_tma, int sms,
+                     int64_t nbat, bool fused, int pair_conc = 0, int quad_conc = 0) {
+  const int fv = g_force_variant.load(std::memory_order_relaxed);
+  const int fb = g_force_bn.load(std::memory_order_relaxed);
+  const int fr = g_force_raster.load(std::memory_order_relaxed);
+  const int fs = g_force_split.load(std::memory_order_relaxed);
+  thread_local TinyCache<13, TilePlan, 8> cache;
+  const uint64_t key[13] = {uint64_t(int64_t(dev)), uint64_t(kind), uint64_t(M), uint64_t(N), uint64_t(K),
+                            uint64_t(es) | (uint64_t(kmajor) << 8) | (uint64_t(all_tma) << 9) | (uint64_t(fused) << 10),
+                            uint64_t(sms), uint64_t(nbat), uint64_t(pair_conc), uint64_t(quad_conc),
+                            (uint64_t(uint32_t(fv)) << 32) | uint32_t(fb), (uint64_t(uint32_t(fr)) << 32) | uint32_t(fs),
+                            0};
+  if (const TilePlan* hit = cache.find(key)) return *hit;
+  const TilePlan plan = choose_plan_uncached(dev, kind, M, N, K, es, kmajor, all_tma, sms, nbat, fused, pair_conc,
+                                             quad_conc, fv, fb, fr, fs);
+  cache.put(key, plan);
+  return plan;
 }
 
 // Strided batch of products (batch = 1: one product; strides in elements).
@@ -550,16 +626,16 @@ int check_arguments(const Call& c) {
 
 // Memory rules that need the device: every pointer is device memory, and C
 // overlaps neither an operand of the batch nor the bias.
-int check_memory(const Call& c) {
+int check_memory(const Call& c, int dev) {
   const int64_t nbat = c.bat.count;
   uintptr_t c0, c1;
   extent(c.C, c.M, c.N, c.ldc, c.eo, &c0, &c1);
   c1 += static_cast<uintptr_t>((nbat - 1) * c.bat.stride_c * c.eo);  // every matrix of the batch
-  if (!is_device_memory(c.C)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+  if (!is_device_memory(c.C, dev)) return GEMM_ERR_NOT_DEVICE_MEMORY;
   if (c.bias != nullptr) {
     const uintptr_t s0 = reinterpret_cast<uintptr_t>(c.bias), s1 = s0 + uintptr_t(c.N) * c.eo;
     if (overlaps(c0, c1, s0, s1)) return GEMM_ERR_INVALID_VALUE;
-    if (!is_device_memory(c.bias)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+    if (!is_device_memory(c.bias, dev)) return GEMM_ERR_NOT_DEVICE_MEMORY;
   }
   if (c.K == 0) return GEMM_OK;
   uintptr_t a0, a1, b0, b1;
@@ -571,7 +647,7 @@ int check_memory(const Call& c) {
   a1 += static_cast<uintptr_t>((nbat - 1) * c.bat.stride_a * c.es);
   b1 += static_cast<uintptr_t>((nbat - 1) * c.bat.stride_b * c.es);
   if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return GEMM_ERR_INVALID_VALUE;
-  if (!is_device_memory(c.A) || !is_device_memory(c.B)) return GEMM_ERR_NOT_DEVICE_MEMORY;
+  if (!is_device_memory(c.A, dev) || !is_device_memory(c.B, dev)) return GEMM_ERR_NOT_DEVICE_MEMORY;
   return GEMM_OK;
 }
 
@@ -805,14 +881,13 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   int st = check_arguments(c);
   if (st != GEMM_OK || M == 0 || N == 0 || bat.count == 0) return st;
   const DeviceInfo* dev = nullptr;
-  st = current_device(&dev);
+  int dev_id = 0;
+  st = current_device(&dev, &dev_id);
   if (st != GEMM_OK) return st;
-  st = check_memory(c);
+  st = check_memory(c, dev_id);
   if (st != GEMM_OK) return st;
   if (K == 0) return run_k_zero(c, dev);
 
-  int dev_id = 0;
-  cudaGetDevice(&dev_id);
   LaunchPlan L;
   memset(&L, 0, sizeof(L));
   GemmParams& p = L.p;
@@ -857,6 +932,7 @@ int run_gemm(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   L.grid = plan.grid;
   L.threads = (p.a_tma && p.b_tma) ? 192 : 320;
   L.stream = c.stream;
+  L.dev = dev_id;
 
   // internal consistency of the derived launch parameters (a violation is a library bug)
   if (p.raster < 1 || p.num_kb < 1 || p.num_tiles < 1 || p.num_work < p.num_tiles || p.tail_segs < 1 ||

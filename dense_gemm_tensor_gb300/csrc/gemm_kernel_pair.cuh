@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(192, 1)
   constexpr int NB = Cf::ACC_BUFS;
   constexpr int CL = 2 * PAIRS;  // CTAs per cluster
   static_assert(PAIRS == 1 || PAIRS == 2, "one pair, or two pairs sharing A");
+  static_assert(PAIRS == 1 || !DGT_NO_MULTICAST, "two pairs share A through a multicast load");
   static_assert(PAIRS == 1 || !Cf::SWAP, "the transposed product runs as single pairs");
 
   extern __shared__ uint8_t smem_raw[];
@@ -274,10 +275,12 @@ __global__ void __launch_bounds__(192, 1)
               if constexpr (PAIRS == 1) {
                 tma_load_3d_pair(a_dst, &tmA, fb, kb * Cf::BK, row0, za);
               } else {
+#if !DGT_NO_MULTICAST
                 // both pairs need these 128 rows of A: each loads 64 of them into
                 // the same place in its own and the other pair's CTA of this half
                 tma_load_3d_pair_mc(a_dst + q * (Cf::A_BYTES / 2), &tmA, fb, kb * Cf::BK, row0 + q * (Cf::BM / 2),
                                     za, uint16_t(0x5u << half));
+#endif
               }
               if constexpr (B_KMAJOR) {
                 tma_load_3d_pair(b_dst, &tmB, fb, kb * Cf::BK, col0, zb);

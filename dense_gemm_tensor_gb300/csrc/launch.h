@@ -23,6 +23,7 @@ struct LaunchPlan {
   int grid;
   int threads;
   cudaStream_t stream;
+  int dev;  // ordinal of the current device
 };
 
 // Kernel launch and co-resident cluster count for one (kind, B layout); each
@@ -82,9 +83,8 @@ constexpr int kPairTileWidths[] = {256, 224, 192, 128};
 template <int KIND, bool KMAJ, int BN>
 cudaError_t launch_variant(const LaunchPlan& L) {
   static int configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  const int dev = L.dev;
+  cudaError_t e;
   auto kern = gemm_kernel<KIND, KMAJ, BN>;
   constexpr int smem = Cfg<KIND, KMAJ, BN>::SMEM_BYTES;
   if (dev >= 64 || !__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
@@ -122,9 +122,8 @@ cudaError_t launch_layout(const LaunchPlan& L) {
 template <int KIND, int OPS, int BN, int PAIRS>
 cudaError_t launch_pair_variant(const LaunchPlan& L) {
   static int configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  const int dev = L.dev;
+  cudaError_t e;
   auto kern = gemm_kernel_pair<KIND, OPS, BN, PAIRS>;
   constexpr int smem = PairCfg<KIND, OPS, BN>::SMEM_BYTES;
   if (dev >= 64 || !__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
@@ -196,7 +195,9 @@ cudaError_t launch_pair_width(const LaunchPlan& L) {
 template <int KIND, int OPS>
 cudaError_t launch_pair_layout(const LaunchPlan& L) {
   if (L.pairs == 1) return launch_pair_width<KIND, OPS, 1>(L);
+#if !DGT_NO_MULTICAST
   if (L.pairs == 2) return launch_pair_width<KIND, OPS, 2>(L);
+#endif
   return cudaErrorInvalidValue;
 }
 
@@ -221,7 +222,8 @@ int pair_clusters_width(int bn) {
   }                                                                                            \
   int pair_clusters_##name(int bn, int pairs) {                                                \
     if (pairs == 1) return pair_clusters_width<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN, 1>(bn);      \
-    if (pairs == 2) return pair_clusters_width<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN, 2>(bn);      \
+    if (pairs == 2 && !DGT_NO_MULTICAST)                                                       \
+      return pair_clusters_width<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN, (DGT_NO_MULTICAST ? 1 : 2)>(bn); \
     return 0;                                                                                  \
   }
 

@@ -5,6 +5,12 @@
 
 #include <stdint.h>
 
+// DGT_NO_MULTICAST=1 builds the library without the cluster-multicast TMA load
+// (and so without the kernel of two CTA pairs that shares A through it).
+#ifndef DGT_NO_MULTICAST
+#define DGT_NO_MULTICAST 0
+#endif
+
 namespace dgt {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -288,8 +294,7 @@ __device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d, uint64_t a, uint64_t
       : "memory");
 }
 
-// Arrive once on the mbarrier at CTA-local offset `bar` in every CTA of
-// `cta_mask` when this thread's earlier pair MMAs have completed.
+#if !DGT_NO_MULTICAST
 // Tiled TMA load multicast to the CTAs of `cta_mask` (the data lands at
 // offset `dst` of each). With .cta_group::2 each destination's completion is
 // signalled on the barrier at the offset of `bar_cluster` in the leader (even
@@ -302,7 +307,10 @@ __device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const void* tm
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
       : "memory");
 }
+#endif
 
+// Arrive once on the mbarrier at CTA-local offset `bar` in every CTA of
+// `cta_mask` when this thread's earlier pair MMAs have completed.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),

@@ -225,7 +225,9 @@ int gemm_e5m2_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, co
  *
  * The first call on each device, with that device current, looks up the
  * array's device address and zeroes its counters (a short synchronous step);
- * make that first call before any stream capture. Every call shares the one
+ * make that first call before any stream capture. If that set-up fails (it
+ * returns GEMM_ERR_LAUNCH, e.g. when tried inside a capture), nothing is
+ * kept and the next call on that device tries it again. Every call shares the one
  * array: calls that overlap on the GPU (different streams, no ordering between
  * them) race on it and may produce wrong results; calls ordered on one stream
  * are safe, since each call's counters are tagged with that call.
@@ -255,7 +257,7 @@ int gemm_reset_device_status(void);
 
 /*
  * Test hooks, process-wide, for subsequent calls. `wait_limit_ns` bounds every
- * wait inside the kernels (0 keeps the default of 1 s). Flag bit 0 makes the
+ * wait inside the kernels (0 keeps the default of 10 s). Flag bit 0 makes the
  * TMA producer issue nothing, so the MMA issuer's first wait runs out: the
  * kernel records a timeout and returns with C unspecified. Flag bit 1 reads
  * operands whose rows TMA cannot address in place with the kernel's copy warps
@@ -283,7 +285,8 @@ int gemm_last_plan(int32_t* out);
  * Tuning hook, process-wide, for subsequent calls. `variant`: 0 = chosen per
  * call, 1 = single-CTA kernel (128-row tiles), 2 = CTA-pair kernel (256-row
  * tiles), 3 = clusters of two CTA pairs that take two adjacent 256-row tiles
- * and load their shared A rows once, by TMA multicast, 4 = CTA-pair kernel
+ * and load their shared A rows once, by TMA multicast (used only in a process
+ * that sees exactly one CUDA device, as every plan with it), 4 = CTA-pair kernel
  * on the transposed product C^T = B^T A^T (TF32, FP16, BF16 with row-major B:
  * 256 columns of C by `tile_n` rows per tile). 2-4 apply only when A and B
  * rows are 16-byte aligned or can be packed, and 4 only with row-major B;

@@ -1,57 +1,48 @@
-"""Host-side logic of bench.py without a GPU: the max-over-ranks reduction
-with two gloo ranks, the reference arm's rank handling, and its JSON line."""
+"""Host-side logic of bench.py without a GPU: the one-GPU rule, the clock
+record and peak choice, the reference arm's rank handling, and its JSON line."""
 
 import json
 import os
-import socket
 import subprocess
 import sys
 
-import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _free_port():
-    s = socket.socket()
-    s.bind(("127.0.0.1", 0))
-    port = s.getsockname()[1]
-    s.close()
-    return port
+def test_ours_refuses_more_than_one_gpu():
+    """The product runs on one GPU: --gpus 2 (or a multi-rank launch) stops
+    with an error before any device work."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 2 and "one GPU" in r.stderr
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "1"], capture_output=True,
+                       text=True, env=env, timeout=300)
+    assert r.returncode == 2 and r.stdout.strip() == ""
 
 
-def _rank_main(rank, world, port, out):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
-    sys.path.insert(0, ROOT)
-    import torch.distributed as dist
-    import bench
-    dist.init_process_group("gloo", rank=rank, world_size=world)
-    try:
-        got = bench.reduce_max(1.5 + rank * 10.0, world)
-        out[rank] = got
-        dist.barrier()
-    finally:
-        dist.destroy_process_group()
-
-
-def test_reduce_max_over_two_gloo_ranks():
-    ctx = mp.get_context("spawn")
-    manager = ctx.Manager()
-    out = manager.dict()
-    port = _free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(120)
-        assert p.exitcode == 0
-    assert dict(out) == {0: 11.5, 1: 11.5}
-
-
-def test_reduce_max_single_process_is_identity():
+def test_clock_window_and_peak_choice():
+    """Samples outside the timed region's host-time window are left out; the
+    burst peak applies only with the median clock at its maximum and no
+    slowdown reason."""
     sys.path.insert(0, ROOT)
     import bench
-    assert bench.reduce_max(3.25, 1) == 3.25
+    s = bench.ClockSampler(0)
+    s.sm_max, s.source = 2070, "nvml"
+    s.samples = [(0.5, 1500, ("sw_power_cap",), 900.0), (1.0, 2070, (), 500.0), (1.1, 2070, (), 600.0),
+                 (1.2, 2055, (), 700.0), (2.5, 1600, ("sw_power_cap",), 1300.0)]
+    d = s.summary(1.0, 2.0)
+    assert d["samples"] == 3 and d["sm_mhz"] == 2070 and d["sm_min_mhz"] == 2055
+    assert d["reasons"] == [] and d["power_w_max"] == 700.0 and d["window_ms"] == 1000.0
+    assert not bench.peak_is_sustained(d)
+    d = s.summary(0.0, 3.0)
+    assert d["reasons"] == ["sw_power_cap"] and bench.peak_is_sustained(d)
+    assert bench.peak_is_sustained(s.summary(5.0, 6.0))  # no samples: the lower, sustained peak
+    assert bench.peak_is_sustained({"sm_mhz": 1700, "sm_max_mhz": 2070, "reasons": []})
+    peaks = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1800.0}
+    assert bench.peak_for("bf16", peaks, False) == 2000.0 and bench.peak_for("bf16", peaks, True) == 1800.0
+    assert abs(bench.peak_for("tf32", peaks, False) - 2000.0 * 1.1 / 2.25) < 1e-9
 
 
 def test_reference_arm_other_ranks_do_no_work():
