@@ -5,8 +5,9 @@ the three 4096^3 products (TF32 with fp32 operands uniform in [-1, 1);
 FP16 and BF16 with N(0, 1) operands), each one launch of the library's
 kernel through its C interface. ``value`` is TFLOP/s (2MNK per product)
 over the timed steps with the operands resident in device memory; ``e2e``
-is the same metric through the host-memory call (pinned host operands copied
-in, C copied out, every step). ``--impl reference`` times the CPU oracle on
+is the same metric through the library's host-memory C call
+(``gemm_{tf32,f16,bf16}_host``: pinned host operands copied in, C copied out,
+every step). ``--impl reference`` times the CPU oracle on
 the same workload instead (a bounded slice of rows per step).
 
 Launch: ``python bench.py [--steps K] [--warmup W]``. The library and this
@@ -387,8 +388,9 @@ def run_ours(args):
                                     f"SM x {SM_COUNT} SMs at the sampled median clock"},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "overlap": "a step's three products are enqueued before the previous step's results are waited "
-                           "for (two buffer sets); every step's copies run inside the timed region"},
+                "call": "gemm_{tf32,f16,bf16}_host (C interface, host pointers)",
+                "overlap": "a step's three calls are enqueued before the previous step's results are waited "
+                           "for; every step's copies run inside the timed region"},
         "clocks": clocks,
         "gpu_launches": launches,
     }

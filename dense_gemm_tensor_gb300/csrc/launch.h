@@ -74,6 +74,10 @@ struct ExternalScratch {
 int run_gemm_external(int kind, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                       int64_t ldb, void* C, int64_t ldc, int layout, void* stream, const ExternalScratch* ext);
 
+// Releases the staging of the host-memory calls (gemm_*_host); the device
+// must be idle.
+int free_host_buffers();
+
 // Tile widths the kernels are built for (the host picks one per call).
 constexpr int kTileWidths[] = {256, 224, 192, 128};
 constexpr int kPairTileWidths[] = {256, 224, 192, 128};

@@ -4,7 +4,7 @@ The functions ``gemm_tf32``, ``gemm_f16`` and ``gemm_bf16`` have the names
 and arguments of the C interface (``include/dgt_gemm.h``) and take raw device
 pointers. ``matmul`` takes torch CUDA tensors and derives sizes, leading
 dimensions and the current stream from them; ``matmul_from_host`` is the
-end-to-end call for operands held in (pinned) host memory. Every step of the
+end-to-end call (``gemm_*_host``) for operands held in (pinned) host memory. Every step of the
 product runs in the library's CUDA kernels; there is no other code path, and
 a missing or unloadable library raises.
 """
@@ -50,7 +50,7 @@ EXPORTS = ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_tf32_ex", "gemm_f16_ex", 
            "gemm_launch_count", "gemm_set_tuning", "gemm_last_plan", "gemm_free_workspaces",
            "gemm_bf16_static_scratch", "gemm_tf32_strided_batched", "gemm_f16_strided_batched",
            "gemm_bf16_strided_batched", "gemm_e4m3_strided_batched", "gemm_e5m2_strided_batched",
-           "gemm_plan_query")
+           "gemm_plan_query", "gemm_tf32_host", "gemm_f16_host", "gemm_bf16_host")
 
 _lib = None
 
@@ -71,7 +71,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         raise RuntimeError(f"{path} is missing: build it with dense_gemm_tensor_gb300.build.build()")
     lib = ctypes.CDLL(path)
     i64, vp, u32, u64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64
-    for name in ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_bf16_static_scratch"):
+    for name in ("gemm_tf32", "gemm_f16", "gemm_bf16", "gemm_bf16_static_scratch", "gemm_tf32_host", "gemm_f16_host",
+                 "gemm_bf16_host"):
         fn = getattr(lib, name)
         fn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int, vp]
         fn.restype = ctypes.c_int
@@ -318,90 +319,63 @@ def bmm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, *, la
     return out
 
 
-_COPY_STREAMS: dict = {}
+_HOST_FN = {torch.float32: "gemm_tf32_host", torch.float16: "gemm_f16_host", torch.bfloat16: "gemm_bf16_host"}
 
 
-def _copy_streams(dev: torch.device) -> tuple:
-    """One host-to-device and one device-to-host stream per device, shared by
-    every end-to-end call, so the copies of consecutive calls queue in call
-    order instead of competing for the host link."""
-    idx = dev.index if dev.index is not None else torch.cuda.current_device()
-    if idx not in _COPY_STREAMS:
-        _COPY_STREAMS[idx] = (torch.cuda.Stream(idx), torch.cuda.Stream(idx))
-    return _COPY_STREAMS[idx]
+def gemm_host(dtype_name, M, N, K, A, lda, B, ldb, C, ldc, layout=GEMM_B_ROW_MAJOR, stream=None) -> int:
+    """gemm_{tf32,f16,bf16}_host with raw host pointers (ints) and a raw stream handle."""
+    return getattr(load(), f"gemm_{dtype_name}_host")(M, N, K, A, lda, B, ldb, C, ldc, layout, stream)
 
 
 def matmul_from_host(A_host: torch.Tensor, B_host: torch.Tensor, *, layout: int = GEMM_B_ROW_MAJOR,
                      device: torch.device | str = "cuda", stream: torch.cuda.Stream | None = None,
-                     buffers: dict | None = None, chunks: int | None = None, wait: bool = True):
-    """End-to-end product of host operands: copy A and B to the device, run
-    the kernels, copy C back into a pinned host tensor.
+                     buffers: dict | None = None, wait: bool = True):
+    """End-to-end product of host operands through the C call
+    gemm_{tf32,f16,bf16}_host: the library copies B and A (in row blocks) to
+    its device staging, runs each block's product as it lands, and copies
+    each block of C back while the next one computes.
 
-    B is copied first; A is then streamed in row blocks: block i's product
-    runs while block i+1 is copied in and block i-1's rows of C are copied out
-    (a copy-in and a copy-out stream shared by all calls on the device, and the
-    compute stream, ordered by events), so the host<->device copies in both
-    directions overlap each other and the kernels. ``chunks`` sets the number
-    of row blocks (default: one per 1024 rows of A, at most 4). ``buffers``
-    (optional, reused across calls) caches the device and pinned host buffers
-    so repeated calls do not allocate.
-
-    With ``wait`` (the default) the call synchronises and returns C. With
-    ``wait=False`` it returns ``(C, event)`` at once: C is valid once ``event``
-    has completed, and the copies of a following call queue behind this one's,
-    so several products can be in flight. A call that reuses ``buffers`` first
-    waits (on the host) for the previous call on them to finish, since it
-    overwrites their contents, C among them. ``A_host`` and ``B_host`` must
-    stay unchanged until the call's event has completed.
+    ``A_host`` / ``B_host``: 2-D CPU tensors (page-locked for the copies to
+    overlap), rows contiguous. The result goes to a page-locked host tensor
+    cached in ``buffers`` (optional, reused across calls of the same shape).
+    With ``wait`` (the default) the call synchronises and returns C; with
+    ``wait=False`` it returns ``(C, event)`` at once, C being valid once
+    ``event`` has completed. A call that reuses ``buffers`` first waits for
+    the previous call on them (it overwrites their C). ``A_host`` and
+    ``B_host`` must stay unchanged until the call's event has completed.
     """
+    dt = A_host.dtype
+    if dt not in _HOST_FN or B_host.dtype != dt:
+        raise TypeError("A and B must both be float32, float16 or bfloat16")
+    if A_host.is_cuda or B_host.is_cuda:
+        raise ValueError("A and B must be host tensors")
     buffers = {} if buffers is None else buffers
     dev = torch.device(device)
-    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    s = stream if stream is not None else torch.cuda.current_stream(idx)
     if buffers.get("done") is not None:
         buffers["done"].synchronize()
-    M = A_host.shape[0]
+    M, K = A_host.shape
     N = B_host.shape[1] if layout == GEMM_B_ROW_MAJOR else B_host.shape[0]
-    out_dtype = torch.bfloat16 if A_host.dtype in _FP8 else A_host.dtype
-    key = (A_host.shape, B_host.shape, A_host.dtype, layout)
+    if (B_host.shape[0] if layout == GEMM_B_ROW_MAJOR else B_host.shape[1]) != K:
+        raise ValueError("B's K dimension does not match A")
+    key = (M, N, dt)
     if buffers.get("key") != key:
-        buffers.update(key=key,
-                       a=torch.empty(A_host.shape, dtype=A_host.dtype, device=dev),
-                       b=torch.empty(B_host.shape, dtype=B_host.dtype, device=dev),
-                       c=torch.empty((M, N), dtype=out_dtype, device=dev),
-                       c_host=torch.empty((M, N), dtype=out_dtype, pin_memory=True))
-    n = chunks if chunks is not None else max(1, min(4, M // 1024))
-    n = max(1, min(n, M)) if M > 0 else 1
-    bounds = [M * i // n for i in range(n + 1)]
-    a, b, c, c_host = buffers["a"], buffers["b"], buffers["c"], buffers["c_host"]
-    s_in, s_out = _copy_streams(dev)
-    start = torch.cuda.Event()
-    start.record(s)
-    s_in.wait_event(start)
-    s_out.wait_event(start)
-    with torch.cuda.stream(s_in):
-        b.copy_(B_host, non_blocking=True)
-    for i in range(n):
-        lo, hi = bounds[i], bounds[i + 1]
-        with torch.cuda.stream(s_in):
-            a[lo:hi].copy_(A_host[lo:hi], non_blocking=True)
-            arrived = torch.cuda.Event()
-            arrived.record(s_in)
-        s.wait_event(arrived)
-        with torch.cuda.stream(s):
-            if hi > lo:
-                matmul(a[lo:hi], b, c[lo:hi], layout=layout, stream=s)
-            computed = torch.cuda.Event()
-            computed.record(s)
-        s_out.wait_event(computed)
-        with torch.cuda.stream(s_out):
-            c_host[lo:hi].copy_(c[lo:hi], non_blocking=True)
+        buffers.update(key=key, c_host=torch.empty((M, N), dtype=dt, pin_memory=True))
+    c = buffers["c_host"]
+    with torch.cuda.device(idx):
+        code = getattr(load(), _HOST_FN[dt])(M, N, K, A_host.data_ptr() or None, _rows(A_host, "A"),
+                                             B_host.data_ptr() or None, _rows(B_host, "B"), c.data_ptr() or None,
+                                             N, layout, s.cuda_stream)
+    if code != GEMM_OK:
+        raise GemmError(code, _HOST_FN[dt])
     done = torch.cuda.Event()
-    done.record(s_out)  # after the last kernel (s_out waited for it) and the last copy out
+    done.record(s)
     buffers["done"] = done
     if wait:
         done.synchronize()
-        return c_host
-    return c_host, done
+        return c
+    return c, done
 
 
 def device_status(stream: torch.cuda.Stream | None = None) -> int:

@@ -235,6 +235,44 @@ int gemm_e5m2_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, co
 int gemm_bf16_static_scratch(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
                              int64_t ldb, uint16_t* C, int64_t ldc, int layout, void* stream);
 
+/*
+ * Products of operands in host memory: gemm_tf32_host, gemm_f16_host,
+ * gemm_bf16_host. The same product, arithmetic and layouts as the device
+ * calls above, but A, B and C are host memory (leading dimensions in
+ * elements as above; C rows receive N elements each). The pages time the
+ * product with its operands already on the GPU; these calls add the copies a
+ * caller holding the matrices on the host needs, and overlap them: B and then
+ * A go to device staging buffers on a copy stream, A in row blocks (up to 4
+ * of at least 1024 rows), each block's product runs on `stream` as soon as
+ * the block has arrived, and each block's rows of C return on a second copy
+ * stream as soon as its product is done.
+ *
+ * Asynchrony: the call enqueues everything and returns; C holds the result
+ * once `stream` has been synchronised (every later operation on `stream`
+ * waits for the last copy of C). The copies of A and B are ordered after
+ * this function's earlier calls on `stream`, not after other work on it, so
+ * A and B must hold their values when the call is made and stay unchanged
+ * until `stream` has reached this call's end. Page-locked host memory
+ * (cudaHostAlloc, cudaHostRegister) lets the copies overlap one another and
+ * the products; pageable memory gives the same result with the copies
+ * waiting for the host.
+ *
+ * Memory: the library keeps two staging slots per (device, stream), taken by
+ * consecutive calls in turn (so one call's uploads can overlap the previous
+ * call's downloads) and grown with cudaMalloc when a call needs more (make
+ * the first call of a size outside stream capture); gemm_free_workspaces
+ * releases them. Errors: the checks of the device calls on sizes, leading
+ * dimensions, layout and element alignment; GEMM_ERR_INVALID_VALUE for an
+ * A, B or C that is device memory (checked before anything is enqueued) or
+ * a copy the runtime refuses; the device call's own codes otherwise.
+ */
+int gemm_tf32_host(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B, int64_t ldb,
+                   float* C, int64_t ldc, int layout, void* stream);
+int gemm_f16_host(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                  uint16_t* C, int64_t ldc, int layout, void* stream);
+int gemm_bf16_host(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B, int64_t ldb,
+                   uint16_t* C, int64_t ldc, int layout, void* stream);
+
 /* Static English text for a return code; never NULL. */
 const char* gemm_status_string(int status);
 
@@ -265,7 +303,8 @@ int gemm_reset_device_status(void);
  */
 int gemm_set_debug(uint32_t flags, uint64_t wait_limit_ns);
 
-/* Waits for the device, then frees every scratch buffer the library holds. */
+/* Waits for the device, then frees every scratch and staging buffer (and the
+ * copy streams of the host-memory calls) the library holds. */
 int gemm_free_workspaces(void);
 
 /* Number of kernels this library has launched in this process. */

@@ -326,23 +326,25 @@ def test_workload_sampled(name):
     print(name, res)
 
 
-@pytest.mark.parametrize("dtype,layout,chunks", [("bf16", 0, None), ("tf32", 1, 3), ("f16", 0, 1)])
-def test_matmul_from_host_pipelined(dtype, layout, chunks):
-    """The end-to-end call on pinned host operands: row blocks of A streamed in,
-    blocks of C streamed out while the next block computes; every entry checked."""
-    M, N, K = 2600, 700, 900
+@pytest.mark.parametrize("dtype,layout,M", [("bf16", 0, 2600), ("tf32", 1, 3100), ("f16", 0, 700)])
+def test_matmul_from_host_pipelined(dtype, layout, M):
+    """The end-to-end call on pinned host operands (gemm_*_host): row blocks of
+    A streamed in (2, 3 and 1 blocks here), blocks of C streamed out while the
+    next block computes; every entry checked."""
+    N, K = 700, 900
     p = inputs.make_problem("host", dtype, M, N, K, layout=layout, seed_a=61, seed_b=62)
     bufs = {}
-    for _ in range(2):  # the second call reuses the cached buffers and streams
-        C = gemm.matmul_from_host(p.a.pin_memory(), p.b.pin_memory(), layout=layout, buffers=bufs, chunks=chunks)
+    for _ in range(2):  # the second call reuses the library's staging and the pinned result
+        C = gemm.matmul_from_host(p.a.pin_memory(), p.b.pin_memory(), layout=layout, buffers=bufs)
     _check_full(p, C)
 
 
 def test_matmul_from_host_many_in_flight():
-    """Three end-to-end products enqueued at once (wait=False): their copies
-    queue on the device's shared copy streams while earlier products compute;
-    every entry of each result checked. A call that reuses a pending call's
-    buffers waits for it, and returns its own product."""
+    """Three end-to-end products enqueued at once (wait=False): they take the
+    stream's two staging slots in turn, so the third waits for the first's
+    products before its uploads; every entry of each result checked. A call
+    that reuses a pending call's result buffer waits for it, and returns its
+    own product."""
     probs = [inputs.make_problem("fly", "tf32", 1500, 900, 700, seed_a=81, seed_b=82),
              inputs.make_problem("fly", "f16", 2100, 640, 1000, layout=1, seed_a=83, seed_b=84),
              inputs.make_problem("fly", "bf16", 3000, 1100, 500, seed_a=85, seed_b=86)]
