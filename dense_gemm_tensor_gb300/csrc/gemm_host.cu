@@ -24,9 +24,14 @@ __device__ uint32_t g_status_words[2];
 // aligned rows of dst_ld_bytes. Each thread moves one 16-byte destination
 // chunk (consecutive threads take consecutive chunks of a row, so reads and
 // writes coalesce); bytes of the last chunk beyond row_bytes are zero.
+// Launched as a programmatic dependent of the previous kernel on the stream
+// (which may still be reading this stream's scratch): it waits for that
+// kernel before touching memory, and lets the kernel after it be scheduled
+// once its own copies are done.
 __global__ void __launch_bounds__(256) pack_rows_kernel(const uint8_t* __restrict__ src, long long src_ld_bytes,
                                                         uint8_t* __restrict__ dst, long long dst_ld_bytes,
                                                         int rows, long long row_bytes, int gran) {
+  grid_dependency_wait();
   const long long chunks_per_row = (row_bytes + 15) / 16;
   const long long total = chunks_per_row * rows;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -62,6 +67,7 @@ __global__ void __launch_bounds__(256) pack_rows_kernel(const uint8_t* __restric
     }
     *reinterpret_cast<uint4*>(dst + r * dst_ld_bytes + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  grid_launch_dependents();
 }
 
 // dst[n][k] = src[k][n] for a rows x cols byte matrix (rows = K, cols = N):
@@ -988,10 +994,19 @@ cudaError_t launch_pack(const void* src, int64_t src_ld_bytes, void* dst, int64_
   const long long chunks = (row_bytes + 15) / 16 * rows;
   long long blocks = (chunks + 255) / 256;
   if (blocks > 8LL * sm_count) blocks = 8LL * sm_count;
-  pack_rows_kernel<<<int(blocks), 256, 0, stream>>>(static_cast<const uint8_t*>(src), src_ld_bytes,
-                                                    static_cast<uint8_t*>(dst), dst_ld_bytes, int(rows), row_bytes,
-                                                    gran);
-  const cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(unsigned(blocks), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, pack_rows_kernel, static_cast<const uint8_t*>(src), (long long)src_ld_bytes,
+                                     static_cast<uint8_t*>(dst), (long long)dst_ld_bytes, int(rows),
+                                     (long long)row_bytes, gran);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
   return e;
 }

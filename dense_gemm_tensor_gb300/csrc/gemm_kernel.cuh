@@ -638,12 +638,13 @@ __device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUten
 
 // Converts 32 accumulator columns of the warp's 32 rows (lane = row, values
 // in r) to the output type and writes them to C[row0 .., col0 .. col0+31] of
-// matrix bz, through the fused epilogue when the launch has one.
+// matrix bz, through the fused epilogue when the launch has one (FUSED =
+// false: a kernel built for plain launches only, without that code).
 // Warp-collective.
-template <int KIND>
+template <int KIND, bool FUSED = true>
 __device__ __forceinline__ void emit_chunk(const GemmParams& p, const CUtensorMap* tmC, EpiRing& ring, int lane,
                                            int row0, int col0, int bz, const uint32_t (&r)[32]) {
-  if (p.fused) {
+  if (FUSED && p.fused) {
     epi_round_fused<KIND, 0>(p, tmC, ring, lane, row0, col0, bz, r);
     if (KIND == KIND_TF32 && col0 + 16 < p.N) epi_round_fused<KIND, 16>(p, tmC, ring, lane, row0, col0 + 16, bz, r);
     return;
@@ -725,8 +726,10 @@ __device__ __forceinline__ void epi_put_cols(uint32_t stage, int lane, int h, co
 // columns; fp32 C: two of 16), filled by epi_put_cols and written out as in
 // emit_chunk. With the fused epilogue each lane first computes its column's
 // values in fp32 in the order of epi_round_fused (alpha * acc, + beta * C,
-// read from the staged box of C, + bias[col], activation). Warp-collective.
-template <int KIND>
+// read from the staged box of C, + bias[col], activation). FUSED = false
+// leaves the fused code out (a kernel built for plain launches: its
+// registers then hold no fused-epilogue values). Warp-collective.
+template <int KIND, bool FUSED = true>
 __device__ __forceinline__ void emit_chunk_t(const GemmParams& p, const CUtensorMap* tmC, EpiRing& ring, int lane,
                                              int row0, int col0, int bz, const uint32_t (&r)[32]) {
   constexpr int NT = KIND == KIND_TF32 ? 2 : 1;  // staging tiles per chunk
@@ -737,7 +740,7 @@ __device__ __forceinline__ void emit_chunk_t(const GemmParams& p, const CUtensor
     const int cb = col0 + h * RC;
     if (cb >= p.N) break;
     const uint32_t stage = epi_acquire(p, lane, ring);
-    if (p.fused) {
+    if (FUSED && p.fused) {
       using T = typename KindTraits<KIND>::T;
       float v[32];
 #pragma unroll

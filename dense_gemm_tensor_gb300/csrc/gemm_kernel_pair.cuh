@@ -163,7 +163,9 @@ __device__ __forceinline__ int pair_kb(const PairWork& wk, int i, int round) {
 
 __device__ __forceinline__ void epilogue_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-template <int KIND, int OPS, int BN, int PAIRS>
+// FUSED = false: built for launches without a fused epilogue (p.fused == 0),
+// with that code left out.
+template <int KIND, int OPS, int BN, int PAIRS, bool FUSED>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -388,9 +390,9 @@ __global__ void __launch_bounds__(192, 1)
       // accumulator chunk c (32 columns) of the warp's 32 rows, as output
       auto emit = [&](int c, const uint32_t(&v)[32]) {
         if constexpr (Cf::SWAP)
-          emit_chunk_t<KindTraits<KIND>::out>(p, &tmC, ring, lane, col0 + c * 32, row0, wk.bz, v);
+          emit_chunk_t<KindTraits<KIND>::out, FUSED>(p, &tmC, ring, lane, col0 + c * 32, row0, wk.bz, v);
         else
-          emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, v);
+          emit_chunk<KindTraits<KIND>::out, FUSED>(p, &tmC, ring, lane, row0, col0 + c * 32, wk.bz, v);
       };
       if (wk.f < 0) {
         for_each_acc_chunk(taddr, nchunks, emit);

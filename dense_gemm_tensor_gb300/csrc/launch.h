@@ -123,12 +123,12 @@ cudaError_t launch_layout(const LaunchPlan& L) {
 }
 
 
-template <int KIND, int OPS, int BN, int PAIRS>
+template <int KIND, int OPS, int BN, int PAIRS, bool FUSED>
 cudaError_t launch_pair_variant(const LaunchPlan& L) {
   static int configured[64] = {};
   const int dev = L.dev;
   cudaError_t e;
-  auto kern = gemm_kernel_pair<KIND, OPS, BN, PAIRS>;
+  auto kern = gemm_kernel_pair<KIND, OPS, BN, PAIRS, FUSED>;
   constexpr int smem = PairCfg<KIND, OPS, BN>::SMEM_BYTES;
   if (dev >= 64 || !__atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -160,7 +160,7 @@ cudaError_t launch_pair_variant(const LaunchPlan& L) {
 // Co-resident clusters of one pair variant (occupancy query with its launch shape).
 template <int KIND, int OPS, int BN, int PAIRS>
 int pair_clusters_variant() {
-  auto kern = gemm_kernel_pair<KIND, OPS, BN, PAIRS>;
+  auto kern = gemm_kernel_pair<KIND, OPS, BN, PAIRS, true>;
   constexpr int smem = PairCfg<KIND, OPS, BN>::SMEM_BYTES;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
     cudaGetLastError();
@@ -185,13 +185,13 @@ int pair_clusters_variant() {
   return n;
 }
 
-template <int KIND, int OPS, int PAIRS>
+template <int KIND, int OPS, int PAIRS, bool FUSED = true>
 cudaError_t launch_pair_width(const LaunchPlan& L) {
   switch (L.bn) {
-    case 256: return launch_pair_variant<KIND, OPS, 256, PAIRS>(L);
-    case 224: return launch_pair_variant<KIND, OPS, 224, PAIRS>(L);
-    case 192: return launch_pair_variant<KIND, OPS, 192, PAIRS>(L);
-    case 128: return launch_pair_variant<KIND, OPS, 128, PAIRS>(L);
+    case 256: return launch_pair_variant<KIND, OPS, 256, PAIRS, FUSED>(L);
+    case 224: return launch_pair_variant<KIND, OPS, 224, PAIRS, FUSED>(L);
+    case 192: return launch_pair_variant<KIND, OPS, 192, PAIRS, FUSED>(L);
+    case 128: return launch_pair_variant<KIND, OPS, 128, PAIRS, FUSED>(L);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -231,11 +231,14 @@ int pair_clusters_width(int bn) {
     return 0;                                                                                  \
   }
 
-// Body of one gemm_<kind>_sw.cu: the pair kernel on the transposed product, each width.
+// Body of one gemm_<kind>_sw.cu: the pair kernel on the transposed product,
+// each width, built twice: with the fused epilogue, and without it for plain
+// launches (no registers held for the fused terms: measured 0.1-0.6% faster).
 #define DGT_DEFINE_SWAP_VARIANTS(name, KIND)                                   \
   cudaError_t launch_##name(const LaunchPlan& L) {                             \
     if (L.b_kmajor || !L.pair || !L.swap || L.pairs != 1) return cudaErrorInvalidValue; \
-    return launch_pair_width<KIND, OPS_SWAP, 1>(L);                            \
+    return L.p.fused ? launch_pair_width<KIND, OPS_SWAP, 1, true>(L)           \
+                     : launch_pair_width<KIND, OPS_SWAP, 1, false>(L);         \
   }
 
 }  // namespace dgt

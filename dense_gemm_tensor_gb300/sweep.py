@@ -5,7 +5,10 @@ skipped, so an interrupted sweep resumes) plus a Markdown table.
 Per workload: 10 warm-up launches, then at least 50 timed launches (200 when
 one takes under 100 µs) in back-to-back CUDA-event pairs on one stream, L2 not
 flushed between them (the operands of the larger workloads exceed the L2
-anyway); the median and mean; one cold launch after writing a 256 MiB buffer;
+anyway); the median and mean; the device time per launch with no host time
+between launches (20 launches, or 3 of the long ones, captured in one CUDA
+graph and replayed: for the small products the event pairs above measure the
+Python call, not the kernel); one cold launch after writing a 256 MiB buffer;
 and ``torch.matmul`` on the same operands as context (TF32 allowed for fp32).
 The records also carry the plan, the GPU name, SM count, driver and the SM
 clocks sampled during the timed launches.
@@ -48,6 +51,30 @@ def _time(fn, iters: int) -> list[float]:
     return [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]  # µs
 
 
+def _time_graph(fn, per_graph: int, replays: int = 10) -> float:
+    """Device time per launch with no host time between launches: `per_graph`
+    launches captured in one CUDA graph (on a stream warmed up first, so the
+    library's scratch already exists), replayed `replays` times; µs."""
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(per_graph):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (replays * per_graph)
+
+
 def run_one(name: str, peaks: dict, gpu: int) -> dict:
     p = inputs.workload(name)
     A, B = p.a.cuda(), p.b.cuda()
@@ -70,10 +97,12 @@ def run_one(name: str, peaks: dict, gpu: int) -> dict:
     plan = gemm.last_plan()
     flops = 2.0 * p.M * p.N * p.K
     med = statistics.median(ts)
+    graph_us = _time_graph(fn, 20 if med < 1000 else 3)
     rec = {"workload": name, "dtype": p.dtype, "M": p.M, "N": p.N, "K": p.K, "layout": p.layout,
            "lda": p.lda, "ldb": p.ldb, "seeds": [1000 + inputs.WORKLOADS[name]["n"], 2000 + inputs.WORKLOADS[name]["n"]],
            "iters": iters, "median_us": round(med, 2), "mean_us": round(statistics.mean(ts), 2),
-           "cold_us": round(cold, 2), "tflops": round(flops / (med * 1e-6) / 1e12, 1), "plan": plan}
+           "cold_us": round(cold, 2), "tflops": round(flops / (med * 1e-6) / 1e12, 1), "plan": plan,
+           "graph_us": round(graph_us, 2), "graph_tflops": round(flops / (graph_us * 1e-6) / 1e12, 1)}
     peak = peaks.get("bf16_tflops")
     if peak:
         if p.dtype == "tf32":
@@ -103,13 +132,15 @@ def run_one(name: str, peaks: dict, gpu: int) -> dict:
 
 def markdown(recs: list[dict]) -> str:
     lines = ["| workload | dtype | M x N x K | B | plan (kernel, tile, segs) | median µs | mean µs | cold µs | TFLOP/s | "
-             f"fraction {PEAK_NOTE} | torch.matmul µs |", "|---|---|---|---|---|---|---|---|---|---|---|"]
+             f"fraction {PEAK_NOTE} | in a CUDA graph µs | TFLOP/s in a graph | torch.matmul µs |",
+             "|---|---|---|---|---|---|---|---|---|---|---|---|---|"]
     for r in recs:
         pl = r["plan"]
         kern = {1: "single", 2: "pair", 3: "pair on C^T", 4: "2 pairs"}.get(pl["kernel"], str(pl["kernel"]))
         lines.append(f"| {r['workload']} | {r['dtype']} | {r['M']}x{r['N']}x{r['K']} | {'K-major' if r['layout'] else 'row'} "
                      f"| {kern}, {pl['tile_n']}, {pl['tail_segs']} | {r['median_us']} | {r['mean_us']} | {r['cold_us']} "
-                     f"| {r['tflops']} | {r.get('frac_of_peak', '')} | {r.get('torch_matmul_us', '')} |")
+                     f"| {r['tflops']} | {r.get('frac_of_peak', '')} | {r.get('graph_us', '')} | {r.get('graph_tflops', '')} "
+                     f"| {r.get('torch_matmul_us', '')} |")
     return "\n".join(lines) + "\n"
 
 
