@@ -426,16 +426,18 @@ KIND_INDEX = {"f16": 0, "bf16": 1, "tf32": 2}
 
 
 def kernel_name(dtype, plan):
-    """The product kernel a plan launches, as ncu names it (row-major B).
+    """The product kernel a plan launches, as ncu names it (row-major B; the
+    last template argument, 0 or 1, is whether it carries the fused epilogue).
     Plan kernel 1: single CTA; 2 and 4: one or two CTA pairs per cluster
     (operand arrangement 0); 3: a CTA pair on the transposed product
-    (arrangement 2), built without the fused epilogue for plain launches."""
+    (arrangement 2). Plain launches of one pair per cluster take the build
+    without the fused epilogue."""
     k, bn = plan["kernel"], plan["tile_n"]
     if k == 1:
         return f"gemm_kernel<{KIND_INDEX[dtype]}, 0, {bn}>"
     if k == 3:
-        return f"gemm_kernel_pair<{KIND_INDEX[dtype]}, 2, {bn}, 1, false>"
-    return f"gemm_kernel_pair<{KIND_INDEX[dtype]}, 0, {bn}, {k // 2}, true>"
+        return f"gemm_kernel_pair<{KIND_INDEX[dtype]}, 2, {bn}, 1, 0>"
+    return f"gemm_kernel_pair<{KIND_INDEX[dtype]}, 0, {bn}, {k // 2}, {0 if k == 2 else 1}>"
 
 
 # Device code of the product kernels: the traffic record holds while these are unchanged.

@@ -79,9 +79,9 @@ def test_kernel_names_and_traffic_record():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.kernel_name("bf16", {"kernel": 1, "tile_n": 256}) == "gemm_kernel<1, 0, 256>"
-    assert bench.kernel_name("tf32", {"kernel": 2, "tile_n": 224}) == "gemm_kernel_pair<2, 0, 224, 1, true>"
-    assert bench.kernel_name("f16", {"kernel": 3, "tile_n": 224}) == "gemm_kernel_pair<0, 2, 224, 1, false>"
-    assert bench.kernel_name("bf16", {"kernel": 4, "tile_n": 256}) == "gemm_kernel_pair<1, 0, 256, 2, true>"
+    assert bench.kernel_name("tf32", {"kernel": 2, "tile_n": 224}) == "gemm_kernel_pair<2, 0, 224, 1, 0>"
+    assert bench.kernel_name("f16", {"kernel": 3, "tile_n": 224}) == "gemm_kernel_pair<0, 2, 224, 1, 0>"
+    assert bench.kernel_name("bf16", {"kernel": 4, "tile_n": 256}) == "gemm_kernel_pair<1, 0, 256, 2, 1>"
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         rec = json.load(f)
     for dt in ("tf32", "f16", "bf16"):
