@@ -196,9 +196,13 @@ cudaError_t launch_pair_width(const LaunchPlan& L) {
   }
 }
 
+// One CTA pair per cluster: built with the fused epilogue and, for plain
+// launches, without it (its registers then hold nothing for the fused terms:
+// no spills); two pairs sharing A: with it only.
 template <int KIND, int OPS>
 cudaError_t launch_pair_layout(const LaunchPlan& L) {
-  if (L.pairs == 1) return launch_pair_width<KIND, OPS, 1>(L);
+  if (L.pairs == 1)
+    return L.p.fused ? launch_pair_width<KIND, OPS, 1, true>(L) : launch_pair_width<KIND, OPS, 1, false>(L);
 #if !DGT_NO_MULTICAST
   if (L.pairs == 2) return launch_pair_width<KIND, OPS, 2>(L);
 #endif
