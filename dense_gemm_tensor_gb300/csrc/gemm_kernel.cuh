@@ -611,17 +611,22 @@ __device__ __forceinline__ void epi_round_fused(const GemmParams& p, const CUten
     __syncwarp();  // every lane has read its row before the tile is overwritten
   }
   if (p.bias != nullptr) {
+    // one load per lane (lane k holds bias[col0 + k]), handed to every lane by shuffles
     const T* bias = static_cast<const T*>(p.bias);
+    float b = 0.0f;
+    if (lane < RC && col0 + lane < p.N) {
+      if constexpr (KIND == KIND_TF32)
+        b = bias[col0 + lane];
+      else if constexpr (KIND == KIND_BF16)
+        b = __bfloat162float(bias[col0 + lane]);
+      else
+        b = __half2float(bias[col0 + lane]);
+    }
 #pragma unroll
-    for (int k = 0; k < RC; ++k)
-      if (col0 + k < p.N) {
-        if constexpr (KIND == KIND_TF32)
-          v[k] += bias[col0 + k];
-        else if constexpr (KIND == KIND_BF16)
-          v[k] += __bfloat162float(bias[col0 + k]);
-        else
-          v[k] += __half2float(bias[col0 + k]);
-      }
+    for (int k = 0; k < RC; ++k) {
+      const float bk = __shfl_sync(0xFFFFFFFFu, b, k);
+      if (col0 + k < p.N) v[k] += bk;
+    }
   }
   epi_activate(v, p.act);
   uint32_t w[16];
