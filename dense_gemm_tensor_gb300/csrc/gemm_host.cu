@@ -415,15 +415,17 @@ struct TilePlan {
 
 // Cycles one SM spends per 128-byte k-slab of a tile in the steady state of
 // the k-loop, by kernel (single CTA, CTA pair, two pairs sharing A) and tile
-// width 256/224/192/128, measured on GB300 at 4096^3 (bf16; tf32 takes the
-// same time per slab). The dense MMA rate alone would give 2 x width; the
+// width 256/224/192/128/64/32, measured on GB300 at 4096^3 (bf16; tf32 takes
+// the same time per slab). The single CTA's 64- and 32-wide entries follow
+// its operand bytes per slab at the SM's intake rate (24 and 20 KB against
+// 32 KB at 128 wide); the pair kernels are not built that narrow. The dense MMA rate alone would give 2 x width; the
 // rest is time the MMA issuer waits for operands. Sharing A between two pairs
 // halves the A bytes each SM fetches from L2 but measured no faster per slab
 // at this size, and its clusters of four leave a few SMs idle.
-constexpr double kSlabCycles[3][4] = {
-    {672.0, 640.0, 605.0, 570.0},  // single CTA, 128 x width tiles
-    {564.0, 504.0, 499.0, 464.0},  // CTA pair, 256 x width tiles
-    {560.0, 503.0, 500.0, 470.0},  // two pairs sharing A, two 256 x width tiles
+constexpr double kSlabCycles[3][6] = {
+    {672.0, 640.0, 605.0, 570.0, 455.0, 380.0},  // single CTA, 128 x width tiles
+    {564.0, 504.0, 499.0, 464.0, 0.0, 0.0},      // CTA pair, 256 x width tiles
+    {560.0, 503.0, 500.0, 470.0, 0.0, 0.0},      // two pairs sharing A, two 256 x width tiles
 };
 // TF32 with row-major B fetches B in 32-column boxes, twice as many as the
 // 16-bit kinds; its pair and shared-A slabs measured 564/542/495/476 cycles,
@@ -448,7 +450,7 @@ constexpr double kSwapTileCycles = 600.0;
 // 32-column boxes per stage at width 256: at 2048^3 it ran 38.6 us where the
 // CTA pair ran 33.4 (BF16: 22.7 and 23.6 us), about 807 cycles per slab
 // against the 16-bit kernel's 672 once the fixed costs are taken out.
-constexpr double kSlabCyclesTf32MnSingle[4] = {807.0, 768.0, 726.0, 684.0};
+constexpr double kSlabCyclesTf32MnSingle[6] = {807.0, 768.0, 726.0, 684.0, 560.0, 470.0};
 
 // Cycles per k-slab of a tile for a kernel family and tile width (wi: index
 // into kTileWidths / kPairTileWidths).
@@ -518,7 +520,7 @@ TilePlan choose_plan_uncached(int dev, int kind, int64_t M, int64_t N, int64_t K
     } else {
       conc = sms;
     }
-    const int wi = bn == 256 ? 0 : bn == 224 ? 1 : bn == 192 ? 2 : 3;
+    const int wi = bn == 256 ? 0 : bn == 224 ? 1 : bn == 192 ? 2 : bn == 128 ? 3 : bn == 64 ? 4 : 5;
     const double slab = slab_cycles(kind, kmajor, pair, pairs, swap, wi);
     const int64_t rows = pair ? 256 : 128;
     const int64_t tiles_n = (nb_ext + bn - 1) / bn;

@@ -330,7 +330,8 @@ int gemm_last_plan(int32_t* out);
  * 256 columns of C by `tile_n` rows per tile). 2-4 apply only when A and B
  * rows are 16-byte aligned or can be packed, and 4 only with row-major B;
  * otherwise the single-CTA kernel runs. `tile_n`: output tile width, 256,
- * 224, 192 or 128 (0 = chosen per call). `raster`: band height of the tile
+ * 224, 192 or 128, and for the single-CTA kernel also 64 or 32 (0 = chosen
+ * per call). `raster`: band height of the tile
  * order in tile rows (0 = chosen per call). `tail_split`: 0 or 2 = split the
  * tiles of the last partial round along K where the shape allows (the
  * default), 1 = never split. Results meet the same accuracy whatever the

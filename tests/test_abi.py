@@ -103,7 +103,10 @@ def test_tuning_hook_validation(lib):
     assert lib.gemm_set_tuning(4, 96, 0, 0) == gemm.GEMM_ERR_INVALID_VALUE
     assert lib.gemm_set_tuning(2, 160, 0, 0) == gemm.GEMM_ERR_INVALID_VALUE   # no 160-wide tile
     assert lib.gemm_set_tuning(3, 96, 0, 0) == gemm.GEMM_ERR_INVALID_VALUE
-    for v, w in ((0, 0), (1, 256), (1, 224), (1, 192), (1, 128), (2, 256), (2, 224), (2, 192), (2, 128), (0, 224),
+    assert lib.gemm_set_tuning(2, 64, 0, 0) == gemm.GEMM_ERR_INVALID_VALUE    # 64 and 32: single CTA only
+    assert lib.gemm_set_tuning(4, 32, 0, 0) == gemm.GEMM_ERR_INVALID_VALUE
+    for v, w in ((0, 0), (1, 256), (1, 224), (1, 192), (1, 128), (1, 64), (1, 32), (0, 64), (2, 256), (2, 224),
+                 (2, 192), (2, 128), (0, 224),
                  (3, 256), (3, 224), (3, 192), (3, 128), (3, 0), (4, 0), (4, 224), (4, 128)):
         assert lib.gemm_set_tuning(v, w, 4, 0) == gemm.GEMM_OK
     assert lib.gemm_set_tuning(0, 0, 0, 0) == gemm.GEMM_OK

@@ -106,3 +106,39 @@ def test_refused_arguments():
     assert gemm.gemm_host("bf16", 8, 8, 8, d.data_ptr(), 8, a.data_ptr(), 8, c.data_ptr(), 8, 0, s) == \
         gemm.GEMM_ERR_INVALID_VALUE
     torch.cuda.synchronize()
+
+
+def test_two_host_threads_on_their_own_streams():
+    """Two host threads, each with its own stream (and so its own staging
+    slots), enqueue host-memory products at the same time; every result is
+    checked."""
+    import threading
+    probs = [inputs.make_problem("hostio3", dt, M, N, K, seed_a=300 + i, seed_b=400 + i)
+             for i, (dt, M, N, K) in enumerate([("bf16", 2048, 320, 520), ("tf32", 1100, 610, 330)])]
+    outs = [None, None]
+    errors = []
+
+    def work(i):
+        try:
+            p = probs[i]
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            a, b = p.a.pin_memory(), p.b.pin_memory()
+            c = torch.empty((p.M, p.N), dtype=TORCH[p.dtype]).pin_memory()
+            for _ in range(3):
+                code = gemm.gemm_host(p.dtype, p.M, p.N, p.K, a.data_ptr(), p.lda, b.data_ptr(), p.ldb, c.data_ptr(),
+                                      p.N, 0, s.cuda_stream)
+                assert code == gemm.GEMM_OK, code
+            s.synchronize()
+            outs[i] = c
+        except Exception as ex:  # noqa: BLE001 - reported below
+            errors.append(ex)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for p, c in zip(probs, outs):
+        _check(p, c, p.N)

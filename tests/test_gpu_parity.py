@@ -114,7 +114,7 @@ def test_small_shapes_transposed_product(dtype, shape):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "tf32"])
 @pytest.mark.parametrize("layout", [0, 1])
-@pytest.mark.parametrize("tile_n", [256, 224, 192, 128])
+@pytest.mark.parametrize("tile_n", [256, 224, 192, 128, 64, 32])
 def test_every_tile_width_full(dtype, layout, tile_n):
     """Each built tile width, forced, on a ragged multi-tile shape (TMA path)
     and on an odd-pitch shape (copy-warp path)."""

@@ -69,7 +69,13 @@ def test_ragged_row_major_b_keeps_the_plain_pair():
 
 
 def test_small_products_and_batches_take_the_single_cta_kernel():
-    assert gemm.plan_query("bf16", 512, 512, 512)["kernel"] == SINGLE
+    # narrow tiles spread a small product over more SMs (CUDA graphs on GB300:
+    # 512^3 5.23 us at 32 wide against 6.17 at 128; 1024^3 8.00 at 64 against
+    # 8.62 at 128 and 12.26 at 32)
+    p = gemm.plan_query("bf16", 512, 512, 512)
+    assert (p["kernel"], p["tile_n"]) == (SINGLE, 32)
+    p = gemm.plan_query("bf16", 1024, 1024, 1024)
+    assert (p["kernel"], p["tile_n"]) == (SINGLE, 64)
     assert gemm.plan_query("bf16", 2048, 2048, 2048)["kernel"] == SINGLE  # 21.2 against 23.2 us
     p = gemm.plan_query("bf16", 512, 512, 512, batch=128)  # 45.8 us against 53.9 on the pair
     assert (p["kernel"], p["tile_n"]) == (SINGLE, 256)
