@@ -431,9 +431,11 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
 // of the 32 x 64-byte box when C's base and row pitch are 16-byte multiples
 // and the box ends at or before column N (TMA leaves out the rows past M; a
 // box that crosses column N wrote whole 16-byte pieces past it on GB300, so
-// that last round of a row goes the other way), otherwise by coalesced stores,
-// 16 lanes to a row and two rows a step, 4 bytes a lane where C's alignment
-// allows and 2 where it does not.
+// that last round of a row goes the other way), otherwise by coalesced stores:
+// where C's addresses are 8-byte multiples and the round's 64 bytes of a row
+// lie inside column N, 8 lanes to a row and four rows a step, 8 bytes a lane;
+// else 16 lanes to a row and two rows a step, 4 bytes a lane where C's
+// alignment allows and 2 where it does not.
 __device__ __forceinline__ uint32_t epi_chunk_addr(uint32_t stage, int r, int j) {
   return stage + static_cast<uint32_t>(r * 64) + (static_cast<uint32_t>(j ^ ((r >> 1) & 3)) << 4);
 }
@@ -486,6 +488,23 @@ __device__ __forceinline__ void epi_flush(const GemmParams& p, const CUtensorMap
       tma_store_3d(tmC, stage, col0, row0, bz);
       bulk_commit_group();
     }
+  } else if (p.c_gran >= 8 && col0 + ROUND_COLS <= p.N) {
+    __syncwarp();
+    constexpr int ES = KIND == KIND_TF32 ? 4 : 2;
+    const int l = lane & 7;  // the lane's 8-byte piece of the row's 64 bytes
+    uint8_t* dst0 = reinterpret_cast<uint8_t*>(p.C) + (bz * p.stride_c + col0) * ES + l * 8;
+#pragma unroll
+    for (int rr = 0; rr < 32; rr += 4) {
+      const int r = rr + (lane >> 3);
+      const int row = row0 + r;
+      uint32_t lo, hi;
+      asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                   : "=r"(lo), "=r"(hi)
+                   : "r"(epi_chunk_addr(stage, r, l >> 1) + ((l & 1) << 3))
+                   : "memory");
+      if (row < p.M) *reinterpret_cast<uint2*>(dst0 + static_cast<long long>(row) * p.ldc * ES) = make_uint2(lo, hi);
+    }
+    __syncwarp();
   } else {
     __syncwarp();
     constexpr int ES = KIND == KIND_TF32 ? 4 : 2;

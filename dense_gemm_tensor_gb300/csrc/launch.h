@@ -53,10 +53,19 @@ cudaError_t launch_transpose_bytes(const void* src, int64_t src_ld, void* dst, i
 // The K = 0 product with a fused epilogue (epilogue_only_kernel).
 cudaError_t launch_epilogue_only(int kind, void* C, long long ldc, int M, int N, const GemmParams& p,
                                  cudaStream_t stream, int sm_count);
-// Copies rows of `row_bytes` from a source with `gran`-byte-aligned row starts
-// to a destination with 16-byte-aligned rows (pack_rows_kernel).
-cudaError_t launch_pack(const void* src, int64_t src_ld_bytes, void* dst, int64_t dst_ld_bytes, int64_t rows,
-                        int64_t row_bytes, int gran, cudaStream_t stream, int sm_count);
+// Copies `rows` rows of `row_bytes` from a source with `gran`-byte-aligned row
+// starts to a destination with 16-byte-aligned rows (pack_rows_kernel); up to
+// two such copies in one launch.
+struct PackSpec {
+  const void* src;
+  int64_t src_ld_bytes;
+  void* dst;
+  int64_t dst_ld_bytes;
+  int64_t rows;
+  int64_t row_bytes;
+  int gran;
+};
+cudaError_t launch_pack(const PackSpec* specs, int n, cudaStream_t stream, int sm_count);
 
 // Split-tail scratch layout: arrival counters (one per CTA of a cluster of up
 // to four) for up to 1024 split work tiles, then the fp32 partial tiles.

@@ -2,6 +2,7 @@
 oracle (oracle/batched.py): every matrix of the batch in full, with the
 single product's acceptance rule (oracle/check.py)."""
 
+import numpy as np
 import pytest
 import torch
 
@@ -180,3 +181,37 @@ def test_batched_fp8(fmt):
     fn = gemm.load().gemm_e4m3_strided_batched
     pa, pc = _dev(a_buf, A).data_ptr(), C.data_ptr()
     assert fn(2, 64, 64, 64, pa, 64, 4096, pa, 64, 4096, pc, 64, 4096, 0, None, None) == gemm.GEMM_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "tf32"])
+@pytest.mark.parametrize("extra", [1, 2, 4])
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+def test_batched_c_stride_granularity(dtype, extra, beta):
+    """C matrices whose batch stride is not a 16-byte multiple (extra elements
+    after each matrix): C is written by row stores no wider than the stride
+    allows, for every matrix of the batch (also when beta * C reads it)."""
+    batch, M, N, K = 3, 130, 200, 96
+    A, a_buf, lda, sa = _batch(dtype, batch, M, K, 300)
+    B, b_buf, ldb, sb = _batch(dtype, batch, K, N, 400)
+    ldc = N + 8
+    sc = M * ldc + extra
+    fill = 0.5
+    Cflat = torch.full((batch * sc + 16,), fill, dtype=TORCH_DT[dtype], device="cuda")
+    C = Cflat.as_strided((batch, M, N), (sc, ldc, 1))
+    gemm.bmm(_dev(a_buf, A), _dev(b_buf, B), C, beta=beta)
+    torch.cuda.synchronize()
+    ref = oracle.gemm_strided_batched(batch, M, N, K, a_buf, lda, sa, b_buf, ldb, sb, 0)
+    s = oracle.abs_gemm_strided_batched(batch, M, N, K, a_buf, lda, sa, b_buf, ldb, sb, 0)
+    got = C.cpu().double().numpy()
+    c_in = np.full((M, N), fill)
+    for z in range(batch):
+        want = oracle.epilogue(ref[z], 1.0, beta, c_in)
+        scale = oracle.epilogue_scale(s[z], 1.0, beta, c_in)
+        res = oracle.check(got[z], want, scale, dtype)
+        assert res["ok"], (z, res)
+    # everything outside the C matrices keeps its value
+    mask = torch.ones(Cflat.numel(), dtype=torch.bool, device="cuda")
+    for z in range(batch):
+        for r in range(M):
+            mask[z * sc + r * ldc:z * sc + r * ldc + N] = False
+    assert torch.all(Cflat[mask] == fill)

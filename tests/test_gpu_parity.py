@@ -219,6 +219,8 @@ def test_small_integers_bit_exact(dtype, layout):
     ("f16", 204, 524, 526),    # 8-byte granularity for A, 4 for B
     ("tf32", 201, 521, 523),   # 4-byte granularity
     ("tf32", 202, 522, 520),   # 8-byte granularity, aligned C
+    ("bf16", 304, 524, 524),   # 8-byte granularity for B and C (8-byte row stores of C)
+    ("tf32", 204, 522, 522),   # the same for fp32
 ])
 @pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("pack", [True, False])
