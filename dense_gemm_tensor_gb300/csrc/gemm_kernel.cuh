@@ -1051,8 +1051,10 @@ __global__ void __launch_bounds__(320, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && ld_volatile_u32(p.status + 1) == p.epoch) {
-    // aborted: let every TMA load that was issued but not consumed land first
+  // Loads issued but not consumed exist only when the launch was aborted: let
+  // them land first. (Comparing the two counts in shared memory keeps the
+  // global abort word, one L2 round trip, off every CTA's exit.)
+  if (threadIdx.x == 0 && *consumed_slot < *issued_slot) {
     const int issued = *issued_slot, consumed = *consumed_slot;
     if (p.a_tma || p.b_tma)
       for (int j = consumed; j < issued; ++j)

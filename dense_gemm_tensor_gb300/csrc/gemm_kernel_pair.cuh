@@ -491,7 +491,9 @@ __global__ void __launch_bounds__(192, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (leader && threadIdx.x == 0 && ld_volatile_u32(p.status + 1) == p.epoch) {
+  // loads issued but not consumed exist only when the launch was aborted
+  // (shared-memory counts: no global read on the normal exit path)
+  if (leader && threadIdx.x == 0 && *consumed_slot < *issued_slot) {
     const int issued = *issued_slot, consumed = *consumed_slot;
     for (int j = consumed; j < issued; ++j)
       if (!wait_phase_drain(p, full0 + 8 * (j % S), (j / S) & 1)) break;
