@@ -424,8 +424,19 @@ int pair_clusters(int dev, int kind, bool kmajor, int bn, int pairs) {
 // at allocation and never reset between calls.
 constexpr int kMaxTailSegs = 4;
 constexpr int kMinSegmentSlabs = 16;         // k-slabs per segment below which splitting does not pay
-constexpr double kSplitPublishCycles = 4000;  // ~2 us at 2 GHz per segment publish/read of a partial
+// ~4 us at 2 GHz per segment for publishing and reading back a partial tile
+// (from measured splits that lost: TF32 2560^3 in three segments 55.6 us
+// against 48.8 unsplit on 192-wide tiles; BF16 12288 x 4096 x 4096 in four
+// 228.7 against 222.9)
+constexpr double kSplitPublishCycles = 8000;
 constexpr double kPairLaunchCycles = 8000;    // extra fixed cost of the pair kernel's launch and set-up
+// The two-pair kernel (clusters of four) costs about 1.2 us more per launch
+// than the plain pair where both run the same rounds (GB300, CUDA graphs:
+// BF16 3072^3 35.2 against 34.1 us, 2048 x 2048 x 8192 44.5 against 43.2,
+// TF32 2048^3 26.8 against 25.8); where its 36 clusters fit the work in whole
+// rounds and the plain pair's 76 pairs do not, it wins (BF16 6144^3, eight
+// rounds either way, 241.5 against 252.5 us).
+constexpr double kTwoPairLaunchCycles = 2500;
 constexpr size_t kCounterBytes = kSplitCounterBytes;  // up to 1024 split tiles
 
 // `ctas`: CTAs per cluster, each publishing its own 128 x bn partial
@@ -607,10 +618,10 @@ TilePlan choose_plan_uncached(int dev, int kind, int64_t M, int64_t N, int64_t K
     }
     const double tile_cost = double(kslabs) * slab + 600.0 + (swap ? kSwapTileCycles : 0.0);
     // a cluster launch with pair set-up costs ~4 us more than a plain one (measured)
-    double cost = double(full) * tile_cost + (pair ? kPairLaunchCycles : 0.0);
+    double cost = double(full) * tile_cost + (pair ? kPairLaunchCycles : 0.0) + (pairs == 2 ? kTwoPairLaunchCycles : 0.0);
     if (rest > 0) {
-      // a split tile also publishes a 128 KiB fp32 partial per CTA (~2 us) and its
-      // last segment reads the other segments' partials back (~2 us each)
+      // a split tile also publishes a 128 KiB fp32 partial per CTA and its last
+      // segment reads the other segments' partials back (kSplitPublishCycles each)
       const double split_cost = tile_cost / segs + kSplitPublishCycles * segs;
       if (segs > 1 && split_cost >= tile_cost) segs = 1;
       cost += segs > 1 ? split_cost : tile_cost;
