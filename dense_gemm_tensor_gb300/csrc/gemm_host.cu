@@ -623,7 +623,7 @@ TilePlan choose_plan_uncached(int dev, int kind, int64_t M, int64_t N, int64_t K
       // a split tile also publishes a 128 KiB fp32 partial per CTA and its last
       // segment reads the other segments' partials back (kSplitPublishCycles each)
       const double split_cost = tile_cost / segs + kSplitPublishCycles * segs;
-      if (segs > 1 && split_cost >= tile_cost) segs = 1;
+      if (segs > 1 && split_cost >= tile_cost && fs != 2) segs = 1;  // (2: split wherever possible)
       cost += segs > 1 ? split_cost : tile_cost;
     }
     if (best_cost < 0 || cost < best_cost) {

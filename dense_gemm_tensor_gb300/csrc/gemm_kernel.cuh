@@ -35,6 +35,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 // A checked build (-DDGT_CHECKED=1) tests, before each shared-memory, tensor
@@ -327,42 +329,21 @@ __device__ __forceinline__ bool warp_wait_phase(const GemmParams& p, uint32_t ba
 }
 
 // ------------------------------------------------------------------ copy warps
-// Copy `bytes` (<= 16, chunk never crosses a 16-byte unit) from global to a
-// swizzled shared-memory position; `valid` bytes come from memory, the rest
-// are zero. Granularity >= 4 uses cp.async, 2 uses a plain load and store.
-__device__ __forceinline__ void copy_chunk(uint32_t dst, const uint8_t* src, int gran, int valid) {
-  if (gran == 16) {
+// Copy one G-byte piece (G = 16, 8, 4: cp.async; 2: a plain load and store)
+// from global to a swizzled shared-memory position; `valid` bytes come from
+// memory, the rest are zero.
+template <int G>
+__device__ __forceinline__ void copy_chunk(uint32_t dst, const uint8_t* src, int valid) {
+  if constexpr (G == 16) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid) : "memory");
-  } else if (gran == 8) {
+  } else if constexpr (G == 8) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(valid) : "memory");
-  } else if (gran == 4) {
+  } else if constexpr (G == 4) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid) : "memory");
   } else {
     uint16_t v = 0;
     if (valid >= 2) v = *reinterpret_cast<const uint16_t*>(src);
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(dst), "h"(v) : "memory");
-  }
-}
-
-// One K-major operand tile: `rows` rows (M or N) of 128 bytes along K.
-// Row r of the tile is global row (row0 + r), bytes from k0 * ES.
-template <int ES>
-__device__ __forceinline__ void copy_kmajor_tile(uint32_t sdst, const uint8_t* base, long long ld_bytes,
-                                                 int rows, int row0, int row_lim, int k0, int K, int gran,
-                                                 int tid) {
-  const int per_row = 128 / gran;
-  const int total = rows * per_row;
-  const long long kbytes_lim = static_cast<long long>(K) * ES;
-  for (int c = tid; c < total; c += 128) {
-    const int r = c / per_row;
-    const int byte = (c - r * per_row) * gran;
-    const uint32_t dst = sdst + r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15));
-    const int grow = row0 + r;
-    const long long gk = static_cast<long long>(k0) * ES + byte;
-    int valid = 0;
-    if (grow < row_lim && gk < kbytes_lim) valid = (kbytes_lim - gk < gran) ? static_cast<int>(kbytes_lim - gk) : gran;
-    const uint8_t* src = valid ? base + grow * ld_bytes + gk : base;
-    copy_chunk(dst, src, gran, valid);
   }
 }
 
@@ -377,26 +358,48 @@ __device__ __forceinline__ uint32_t swz_pos(int k, int byte) {
     return (((byte >> 4) ^ (k & 7)) << 4) | (byte & 15);
 }
 
-// One MN-major B tile: NBOX boxes, each BK rows (K) of 128 bytes along N.
-template <int ES, int BK, int NBOX, int BOX_BYTES, bool ATOM32>
-__device__ __forceinline__ void copy_mnmajor_tile(uint32_t sdst, const uint8_t* base, long long ld_bytes, int n0,
-                                                  int N, int k0, int K, int gran, int tid) {
-  const int per_row = 128 / gran;
-  const int total = NBOX * BK * per_row;
-  const long long nbytes_lim = static_cast<long long>(N) * ES;
-  for (int c = tid; c < total; c += 128) {
-    const int row = c / per_row;  // box * BK + k
-    const int byte = (c - row * per_row) * gran;
-    const int box = row / BK;
-    const int k = row - box * BK;
-    const uint32_t dst = sdst + box * BOX_BYTES + k * 128 + swz_pos<ATOM32>(k, byte);
-    const int gk = k0 + k;
-    const long long gn = static_cast<long long>(n0) * ES + box * 128 + byte;
-    int valid = 0;
-    if (gk < K && gn < nbytes_lim) valid = (nbytes_lim - gn < gran) ? static_cast<int>(nbytes_lim - gn) : gran;
-    const uint8_t* src = valid ? base + gk * ld_bytes + gn : base;
-    copy_chunk(dst, src, gran, valid);
+// `n` 128-byte rows of a swizzled tile (row r of the tile at sdst + r * 128)
+// from global rows grow0 + r, bytes [colb, colb + 128) of each: rows at or
+// past grow_lim and bytes at or past col_lim read as zero. The 128 copy
+// threads each keep one G-byte column of the rows (128 / G threads to a row,
+// G rows a pass for G = 16... 2 per pass), so a thread's column offset and
+// its zero-fill at the right edge are worked out once, and each further row
+// costs an address step and one copy.
+template <int G, bool ATOM32>
+__device__ __forceinline__ void copy_rows(uint32_t sdst, int n, const uint8_t* base, long long ld_bytes, int grow0,
+                                          int grow_lim, long long colb, long long col_lim, int tid) {
+  constexpr int TPR = 128 / G;   // threads per row
+  constexpr int RPP = 128 / TPR; // rows per pass
+  const int r0 = tid / TPR;
+  const int byte = (tid % TPR) * G;
+  const long long cb = colb + byte;
+  const int valid_c = cb >= col_lim ? 0 : (col_lim - cb < G ? static_cast<int>(col_lim - cb) : G);
+  const uint8_t* src = base + static_cast<long long>(grow0 + r0) * ld_bytes + cb;
+  const long long step = static_cast<long long>(RPP) * ld_bytes;
+#pragma unroll 2
+  for (int r = r0; r < n; r += RPP, src += step) {
+    const int valid = grow0 + r < grow_lim ? valid_c : 0;
+    copy_chunk<G>(sdst + r * 128 + swz_pos<ATOM32>(r, byte), valid ? src : base, valid);
   }
+}
+
+// One K-major operand tile: `rows` rows (M or N) of 128 bytes along K.
+// Row r of the tile is global row (row0 + r), bytes from k0 * ES.
+template <int G, int ES>
+__device__ __forceinline__ void copy_kmajor_tile(uint32_t sdst, const uint8_t* base, long long ld_bytes, int rows,
+                                                 int row0, int row_lim, int k0, int K, int tid) {
+  copy_rows<G, false>(sdst, rows, base, ld_bytes, row0, row_lim, static_cast<long long>(k0) * ES,
+                      static_cast<long long>(K) * ES, tid);
+}
+
+// One MN-major B tile: NBOX boxes, each BK rows (K) of 128 bytes along N.
+template <int G, int ES, int BK, int NBOX, int BOX_BYTES, bool ATOM32>
+__device__ __forceinline__ void copy_mnmajor_tile(uint32_t sdst, const uint8_t* base, long long ld_bytes, int n0,
+                                                  int N, int k0, int K, int tid) {
+#pragma unroll 1
+  for (int box = 0; box < NBOX; ++box)
+    copy_rows<G, ATOM32>(sdst + box * BOX_BYTES, BK, base, ld_bytes, k0, K,
+                         static_cast<long long>(n0) * ES + box * 128, static_cast<long long>(N) * ES, tid);
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -1016,17 +1019,28 @@ __global__ void __launch_bounds__(320, 1)
           ok = false;
           break;
         }
-        if (!p.a_tma)
-          copy_kmajor_tile<Cf::ES>(sA + s * Cf::A_BYTES, Ab, lda_b, Cf::BM, mb * Cf::BM, p.M, kb * Cf::BK, p.K,
-                                   p.copy_bytes, ctid);
-        if (!p.b_tma) {
-          if constexpr (B_KMAJOR)
-            copy_kmajor_tile<Cf::ES>(sB + s * Cf::B_BYTES, Bb, ldb_b, Cf::BN, nb * Cf::BN, p.N, kb * Cf::BK, p.K,
-                                     p.copy_bytes, ctid);
-          else
-            copy_mnmajor_tile<Cf::ES, Cf::BK, Cf::NBOX, Cf::BOX_BYTES, Cf::B_ATOM32>(sB + s * Cf::B_BYTES, Bb, ldb_b,
-                                                                        nb * Cf::BN, p.N, kb * Cf::BK, p.K,
-                                                                        p.copy_bytes, ctid);
+        auto copy_stage = [&](auto g) {
+          constexpr int G = decltype(g)::value;
+          if (!p.a_tma)
+            copy_kmajor_tile<G, Cf::ES>(sA + s * Cf::A_BYTES, Ab, lda_b, Cf::BM, mb * Cf::BM, p.M, kb * Cf::BK, p.K,
+                                        ctid);
+          if (!p.b_tma) {
+            if constexpr (B_KMAJOR)
+              copy_kmajor_tile<G, Cf::ES>(sB + s * Cf::B_BYTES, Bb, ldb_b, Cf::BN, nb * Cf::BN, p.N, kb * Cf::BK,
+                                          p.K, ctid);
+            else
+              copy_mnmajor_tile<G, Cf::ES, Cf::BK, Cf::NBOX, Cf::BOX_BYTES, Cf::B_ATOM32>(
+                  sB + s * Cf::B_BYTES, Bb, ldb_b, nb * Cf::BN, p.N, kb * Cf::BK, p.K, ctid);
+          }
+        };
+        // the copy granularity is the same for every stage of the launch
+        switch (p.copy_bytes) {
+          case 16: copy_stage(std::integral_constant<int, 16>{}); break;
+          case 8: copy_stage(std::integral_constant<int, 8>{}); break;
+          case 4: copy_stage(std::integral_constant<int, 4>{}); break;
+          default:
+            if constexpr (Cf::ES == 2) copy_stage(std::integral_constant<int, 2>{});
+            break;
         }
         cp_async_commit();
         if (it >= Cf::COPY_LAG) {

@@ -332,9 +332,10 @@ int gemm_last_plan(int32_t* out);
  * otherwise the single-CTA kernel runs. `tile_n`: output tile width, 256,
  * 224, 192 or 128, and for the single-CTA kernel also 64 or 32 (0 = chosen
  * per call). `raster`: band height of the tile
- * order in tile rows (0 = chosen per call). `tail_split`: 0 or 2 = split the
- * tiles of the last partial round along K where the shape allows (the
- * default), 1 = never split. Results meet the same accuracy whatever the
+ * order in tile rows (0 = chosen per call). `tail_split`: 0 = split the tiles
+ * of the last partial round along K where the cost model expects a gain (the
+ * default), 2 = split them wherever the tile geometry allows (2-4 segments of
+ * at least 16 k-slabs), 1 = never split. Results meet the same accuracy whatever the
  * setting (their bits may differ: the order of the sum over K depends on the
  * plan); each setting is deterministic. Returns GEMM_ERR_INVALID_VALUE for
  * values outside these sets.

@@ -41,7 +41,7 @@ def _extra(dtype, M, N, seed):
     return c_in, bias
 
 
-def _run_and_check(p, alpha, beta, use_bias, act, ldc=None, variant=0, tile_n=0):
+def _run_and_check(p, alpha, beta, use_bias, act, ldc=None, variant=0, tile_n=0, split=0):
     A, B = p.a.cuda(), p.b.cuda()
     a = A[:, :p.K]
     b = B[:, :p.N] if p.layout == 0 else B[:, :p.K]
@@ -50,7 +50,7 @@ def _run_and_check(p, alpha, beta, use_bias, act, ldc=None, variant=0, tile_n=0)
     Cbuf = torch.full((p.M + 2, ldc), 7.0, dtype=TORCH_DT[p.dtype], device="cuda")
     C = Cbuf[:p.M, :p.N]
     C.copy_(c_in.cuda())
-    gemm.set_tuning(variant, tile_n, 0, 0)
+    gemm.set_tuning(variant, tile_n, 0, split)
     try:
         gemm.matmul(a, b, C, layout=p.layout, alpha=alpha, beta=beta,
                     bias=bias.cuda() if use_bias else None, activation=None if act == "none" else act)
@@ -94,7 +94,7 @@ def test_fused_epilogue_terms(dtype, beta, use_bias):
 def test_fused_epilogue_split_tail(dtype, variant):
     """Split tiles: the epilogue applies once, to the summed segments."""
     p = inputs.make_problem("epi3", dtype, 768, 2560, 4096, seed_a=31, seed_b=32, dist_a="normal")
-    _run_and_check(p, alpha=0.5, beta=1.0, use_bias=True, act="relu", variant=variant, tile_n=256)
+    _run_and_check(p, alpha=0.5, beta=1.0, use_bias=True, act="relu", variant=variant, tile_n=256, split=2)
     assert gemm.last_plan()["tail_segs"] > 1
 
 

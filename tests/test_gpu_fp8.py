@@ -34,14 +34,14 @@ def _decoded(p):
     return oracle.decode_fp8(p.a, p.dtype), oracle.decode_fp8(p.b, p.dtype)
 
 
-def _run(p, ldc=None, variant=0, tile_n=0, **epi):
+def _run(p, ldc=None, variant=0, tile_n=0, split=0, **epi):
     A, B = p.a.cuda(), p.b.cuda()
     a = A[:, :p.K]
     b = B[:, :p.N] if p.layout == 0 else B[:, :p.K]
     ldc = p.N if ldc is None else ldc
     Cbuf = torch.full((p.M + 1, ldc), 5.0, dtype=torch.bfloat16, device="cuda")
     C = Cbuf[:p.M, :p.N]
-    gemm.set_tuning(variant, tile_n, 0, 0)
+    gemm.set_tuning(variant, tile_n, 0, split)
     try:
         gemm.matmul(a, b, C, layout=p.layout, **epi)
         torch.cuda.synchronize()
@@ -94,7 +94,7 @@ def test_fp8_unaligned_rows_and_c(fmt):
 @pytest.mark.parametrize("variant", [2, 3])
 def test_fp8_split_tail(fmt, variant):
     p = inputs.make_problem("f8s", fmt, 768, 2560, 4096, layout=1, seed_a=91, seed_b=92, dist_a="normal")
-    C = _run(p, variant=variant, tile_n=256)
+    C = _run(p, variant=variant, tile_n=256, split=2)
     assert gemm.last_plan()["tail_segs"] > 1
     _check(p, C)
 

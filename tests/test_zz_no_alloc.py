@@ -61,9 +61,10 @@ def _reference_plan(p):
 
 
 # (M, N, K, splits): the two split shapes take the CTA pair on the transposed
-# product (three K segments per split tile, 13.8 MB of partials) and the plain
-# CTA pair (two segments, 16.5 MB: just inside the array); the others split nothing.
-SHAPES = [(1792, 3072, 4096, True), (2048, 3072, 4096, True), (4096, 4096, 4096, False), (300, 520, 200, False)]
+# product (192-row tiles, two K segments per split tile, 13.5 MiB of partials)
+# and the plain CTA pair (224-wide tiles, two segments, 15.75 MiB: just inside
+# the array); the others split nothing.
+SHAPES = [(1024, 1536, 6144, True), (768, 2560, 6144, True), (4096, 4096, 4096, False), (300, 520, 200, False)]
 
 
 @pytest.mark.parametrize("M,N,K,splits", SHAPES)
@@ -98,7 +99,7 @@ def test_matches_oracle_on_two_calls(M, N, K, splits):
 def test_plan_beyond_the_array_is_refused():
     """A plan whose split partials exceed the 16 MiB is refused with
     GEMM_ERR_SCRATCH_LIMIT before anything is launched."""
-    M, N, K = 2560, 2560, 4096  # CTA pair, 256-wide tiles, three segments: 18 MiB of partials
+    M, N, K = 768, 3072, 6144  # CTA pair, 256-wide tiles, two segments: 18 MiB of partials
     p = inputs.make_problem("noalloc_big", "bf16", M, N, K, seed_a=11, seed_b=12)
     plan, A, B = _reference_plan(p)
     assert split_bytes(plan) > SCRATCH_BYTES, plan
