@@ -1,0 +1,9 @@
+// BF16, K-major B: the two-pair kernels (A shared by multicast) of this operand kind and layout.
+#include "launch.h"
+namespace dgt {
+#if !DGT_NO_MULTICAST
+DGT_DEFINE_QUAD_VARIANTS(bf16_km, KIND_BF16, true)
+#else
+DGT_DEFINE_NO_QUAD(bf16_km)
+#endif
+}  // namespace dgt

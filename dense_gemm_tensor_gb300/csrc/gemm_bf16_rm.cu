@@ -1,4 +1,4 @@
-// BF16, row-major B: every GEMM kernel instantiation of this operand kind and layout.
+// BF16, row-major B: the single-CTA kernels of this operand kind and layout.
 #include "launch.h"
 namespace dgt {
 DGT_DEFINE_VARIANTS(bf16_rm, KIND_BF16, false)

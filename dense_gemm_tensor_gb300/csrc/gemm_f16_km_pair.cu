@@ -1,0 +1,5 @@
+// FP16, K-major B: the CTA-pair kernels of this operand kind and layout.
+#include "launch.h"
+namespace dgt {
+DGT_DEFINE_PAIR_VARIANTS(f16_km, KIND_F16, true)
+}  // namespace dgt

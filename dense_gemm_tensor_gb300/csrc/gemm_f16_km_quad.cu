@@ -1,0 +1,9 @@
+// FP16, K-major B: the two-pair kernels (A shared by multicast) of this operand kind and layout.
+#include "launch.h"
+namespace dgt {
+#if !DGT_NO_MULTICAST
+DGT_DEFINE_QUAD_VARIANTS(f16_km, KIND_F16, true)
+#else
+DGT_DEFINE_NO_QUAD(f16_km)
+#endif
+}  // namespace dgt

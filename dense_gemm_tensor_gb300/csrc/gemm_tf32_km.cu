@@ -1,4 +1,4 @@
-// TF32, K-major B: every GEMM kernel instantiation of this operand kind and layout.
+// TF32, K-major B: the single-CTA kernels of this operand kind and layout.
 #include "launch.h"
 namespace dgt {
 DGT_DEFINE_VARIANTS(tf32_km, KIND_TF32, true)

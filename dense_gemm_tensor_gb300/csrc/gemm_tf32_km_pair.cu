@@ -1,0 +1,5 @@
+// TF32, K-major B: the CTA-pair kernels of this operand kind and layout.
+#include "launch.h"
+namespace dgt {
+DGT_DEFINE_PAIR_VARIANTS(tf32_km, KIND_TF32, true)
+}  // namespace dgt

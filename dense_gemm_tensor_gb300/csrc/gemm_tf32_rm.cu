@@ -1,4 +1,4 @@
-// TF32, row-major B: every GEMM kernel instantiation of this operand kind and layout.
+// TF32, row-major B: the single-CTA kernels of this operand kind and layout.
 #include "launch.h"
 namespace dgt {
 DGT_DEFINE_VARIANTS(tf32_rm, KIND_TF32, false)

@@ -26,13 +26,17 @@ struct LaunchPlan {
   int dev;  // ordinal of the current device
 };
 
-// Kernel launch and co-resident cluster count for one (kind, B layout); each
-// pair is defined in its own translation unit (gemm_<kind>_<layout>.cu, built
-// in parallel). The FP8 kinds exist for K-major B only (a row-major B is
-// transposed into scratch first).
-#define DGT_DECLARE_VARIANTS(name)                 \
-  cudaError_t launch_##name(const LaunchPlan& L);  \
-  int pair_clusters_##name(int bn, int pairs);
+// Kernel launch and co-resident cluster count for one (kind, B layout): the
+// single-CTA kernels in gemm_<kind>_<layout>.cu, the CTA-pair kernels in
+// gemm_<kind>_<layout>_pair.cu and the two-pair kernels in
+// gemm_<kind>_<layout>_quad.cu, so that the units build in parallel. The FP8 kinds exist for K-major B only (a row-major B
+// is transposed into scratch first).
+#define DGT_DECLARE_VARIANTS(name)                       \
+  cudaError_t launch_##name(const LaunchPlan& L);        \
+  cudaError_t launch_##name##_pair(const LaunchPlan& L); \
+  cudaError_t launch_##name##_quad(const LaunchPlan& L); \
+  int pair_clusters_##name(int bn, int pairs);           \
+  int quad_clusters_##name(int bn);
 DGT_DECLARE_VARIANTS(f16_rm)
 DGT_DECLARE_VARIANTS(f16_km)
 DGT_DECLARE_VARIANTS(bf16_rm)
@@ -212,15 +216,11 @@ cudaError_t launch_pair_width(const LaunchPlan& L) {
 
 // One CTA pair per cluster: built with the fused epilogue and, for plain
 // launches, without it (its registers then hold nothing for the fused terms:
-// no spills); two pairs sharing A: with it only.
+// no spills); two pairs sharing A (their own unit): with it only.
 template <int KIND, int OPS>
 cudaError_t launch_pair_layout(const LaunchPlan& L) {
-  if (L.pairs == 1)
-    return L.p.fused ? launch_pair_width<KIND, OPS, 1, true>(L) : launch_pair_width<KIND, OPS, 1, false>(L);
-#if !DGT_NO_MULTICAST
-  if (L.pairs == 2) return launch_pair_width<KIND, OPS, 2>(L);
-#endif
-  return cudaErrorInvalidValue;
+  if (L.pairs != 1) return cudaErrorInvalidValue;
+  return L.p.fused ? launch_pair_width<KIND, OPS, 1, true>(L) : launch_pair_width<KIND, OPS, 1, false>(L);
 }
 
 template <int KIND, int OPS, int PAIRS>
@@ -234,20 +234,41 @@ int pair_clusters_width(int bn) {
   }
 }
 
-// Body of one gemm_<kind>_<layout>.cu: instantiates every kernel of that kind
-// and B layout (single CTA, CTA pair, two pairs; each tile width).
+// Body of one gemm_<kind>_<layout>.cu: the single-CTA kernels of that kind
+// and B layout, each tile width; pair plans go to launch_<name>_pair.
 #define DGT_DEFINE_VARIANTS(name, KIND, KMAJ)                                                  \
   cudaError_t launch_##name(const LaunchPlan& L) {                                             \
     if (L.b_kmajor != (KMAJ) || L.swap) return cudaErrorInvalidValue;                          \
-    return L.pair ? launch_pair_layout<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN>(L)                   \
-                  : launch_layout<KIND, KMAJ>(L);                                              \
+    return L.pair ? launch_##name##_pair(L) : launch_layout<KIND, KMAJ>(L);                    \
+  }
+
+// Body of one gemm_<kind>_<layout>_pair.cu: the CTA-pair kernels of that
+// kind and B layout, each tile width, with and without the fused epilogue;
+// two-pair plans go to launch_<name>_quad.
+#define DGT_DEFINE_PAIR_VARIANTS(name, KIND, KMAJ)                                             \
+  cudaError_t launch_##name##_pair(const LaunchPlan& L) {                                      \
+    if (L.b_kmajor != (KMAJ) || L.swap || !L.pair) return cudaErrorInvalidValue;               \
+    if (L.pairs == 2) return launch_##name##_quad(L);                                          \
+    return launch_pair_layout<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN>(L);                           \
   }                                                                                            \
   int pair_clusters_##name(int bn, int pairs) {                                                \
     if (pairs == 1) return pair_clusters_width<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN, 1>(bn);      \
-    if (pairs == 2 && !DGT_NO_MULTICAST)                                                       \
-      return pair_clusters_width<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN, (DGT_NO_MULTICAST ? 1 : 2)>(bn); \
+    if (pairs == 2) return quad_clusters_##name(bn);                                           \
     return 0;                                                                                  \
   }
+
+// Body of one gemm_<kind>_<layout>_quad.cu: the two-pair kernels (two CTA
+// pairs sharing A by TMA multicast), each tile width; a build without
+// multicast defines the same two calls without them (DGT_DEFINE_NO_QUAD).
+#define DGT_DEFINE_QUAD_VARIANTS(name, KIND, KMAJ)                                             \
+  cudaError_t launch_##name##_quad(const LaunchPlan& L) {                                      \
+    if (L.b_kmajor != (KMAJ) || L.swap || !L.pair || L.pairs != 2) return cudaErrorInvalidValue; \
+    return launch_pair_width<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN, 2>(L);                         \
+  }                                                                                            \
+  int quad_clusters_##name(int bn) { return pair_clusters_width<KIND, (KMAJ) ? OPS_B_K : OPS_B_MN, 2>(bn); }
+#define DGT_DEFINE_NO_QUAD(name)                                                               \
+  cudaError_t launch_##name##_quad(const LaunchPlan&) { return cudaErrorInvalidValue; }        \
+  int quad_clusters_##name(int) { return 0; }
 
 // Body of one gemm_<kind>_sw.cu: the pair kernel on the transposed product,
 // each width, built twice: with the fused epilogue, and without it for plain

@@ -91,6 +91,16 @@ def test_fp8_unaligned_rows_and_c(fmt):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_row_major_b_with_unaligned_a(fmt):
+    """A with odd rows (packed) and a row-major B (transposed into K-major
+    rows) in the same call: the pack and the transpose both write the
+    stream's scratch, in separate slots."""
+    p = inputs.make_problem("f8r", fmt, 300, 260, 520, layout=0, lda=523, ldb=265, seed_a=85, seed_b=86)
+    C = _run(p, ldc=263)
+    _check(p, C)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("variant", [2, 3])
 def test_fp8_split_tail(fmt, variant):
     p = inputs.make_problem("f8s", fmt, 768, 2560, 4096, layout=1, seed_a=91, seed_b=92, dist_a="normal")
