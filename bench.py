@@ -430,11 +430,11 @@ def kernel_name(dtype, plan):
     last template argument, 0 or 1, is whether it carries the fused epilogue).
     Plan kernel 1: single CTA; 2 and 4: one or two CTA pairs per cluster
     (operand arrangement 0); 3: a CTA pair on the transposed product
-    (arrangement 2). Plain launches of one pair per cluster take the build
-    without the fused epilogue."""
+    (arrangement 2). Plain launches of the single-CTA kernel and of one pair
+    per cluster take the builds without the fused epilogue."""
     k, bn = plan["kernel"], plan["tile_n"]
     if k == 1:
-        return f"gemm_kernel<{KIND_INDEX[dtype]}, 0, {bn}>"
+        return f"gemm_kernel<{KIND_INDEX[dtype]}, 0, {bn}, 0>"
     if k == 3:
         return f"gemm_kernel_pair<{KIND_INDEX[dtype]}, 2, {bn}, 1, 0>"
     return f"gemm_kernel_pair<{KIND_INDEX[dtype]}, 0, {bn}, {k // 2}, {0 if k == 2 else 1}>"

@@ -832,7 +832,9 @@ __device__ __forceinline__ void for_each_acc_chunk(uint32_t taddr, int nchunks, 
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int KIND, bool B_KMAJOR, int BN>
+// FUSED = false: built for launches without a fused epilogue (p.fused == 0),
+// with that code left out.
+template <int KIND, bool B_KMAJOR, int BN, bool FUSED>
 __global__ void __launch_bounds__(320, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
@@ -991,7 +993,7 @@ __global__ void __launch_bounds__(320, 1)
       int ncols = min(Cf::BN, p.N - nb * Cf::BN);
       if (!in_range(p, b * Cf::ACC_COLS + ((ncols + 31) / 32) * 32 <= Cf::TMEM_COLS, CHECK_TMEM_LD)) ncols = 0;
       for_each_acc_chunk(taddr, (ncols + 31) / 32, [&](int c, const uint32_t(&r)[32]) {
-        emit_chunk<KindTraits<KIND>::out>(p, &tmC, ring, lane, row0, nb * Cf::BN + c * 32, bz, r);
+        emit_chunk<KindTraits<KIND>::out, FUSED>(p, &tmC, ring, lane, row0, nb * Cf::BN + c * 32, bz, r);
       });
       tc_fence_before();
       __syncwarp();

@@ -78,7 +78,7 @@ def test_kernel_names_and_traffic_record():
     the plans it was captured with and carries the device sources' hash."""
     sys.path.insert(0, ROOT)
     import bench
-    assert bench.kernel_name("bf16", {"kernel": 1, "tile_n": 256}) == "gemm_kernel<1, 0, 256>"
+    assert bench.kernel_name("bf16", {"kernel": 1, "tile_n": 256}) == "gemm_kernel<1, 0, 256, 0>"
     assert bench.kernel_name("tf32", {"kernel": 2, "tile_n": 224}) == "gemm_kernel_pair<2, 0, 224, 1, 0>"
     assert bench.kernel_name("f16", {"kernel": 3, "tile_n": 224}) == "gemm_kernel_pair<0, 2, 224, 1, 0>"
     assert bench.kernel_name("bf16", {"kernel": 4, "tile_n": 256}) == "gemm_kernel_pair<1, 0, 256, 2, 1>"
