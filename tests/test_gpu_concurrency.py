@@ -34,10 +34,22 @@ def _check(p, C):
     assert res["ok"], res
 
 
+# shapes whose plans split tiles (partials in the per-stream scratch): the
+# plain CTA pair and the pair on the transposed product
+SPLIT_SHAPES = [(768, 1024, 8192), (1024, 1536, 6144)]
+
+
+def test_split_shapes_still_split():
+    for sh in SPLIT_SHAPES:
+        assert gemm.plan_query("bf16", *sh)["tail_segs"] > 1, sh
+
+
 def test_threads_with_their_own_streams():
-    # shapes whose plans split tiles (per-stream scratch) and ones that do not
-    shapes = [(768, 2560, 4096), (1000, 1500, 700), (300, 520, 200), (1280, 1024, 4096)]
-    probs = [inputs.make_problem(f"thr{i}", "bf16", *sh, seed_a=10 + i, seed_b=20 + i, dist_a="normal")
+    # two split plans, one plain, and one whose A rows (odd pitch) are packed
+    # into the stream's scratch first
+    shapes = [SPLIT_SHAPES[0], (1000, 1500, 700), (300, 520, 200), SPLIT_SHAPES[1]]
+    probs = [inputs.make_problem(f"thr{i}", "bf16", *sh, seed_a=10 + i, seed_b=20 + i, dist_a="normal",
+                                 lda=sh[2] + 3 if i == 2 else None)
              for i, sh in enumerate(shapes)]
     outs = [None] * len(probs)
     errors = []
@@ -48,7 +60,7 @@ def test_threads_with_their_own_streams():
             s = torch.cuda.Stream()
             p = probs[i]
             with torch.cuda.stream(s):
-                A, B = p.a.cuda(), p.b.cuda()
+                A, B = p.a.cuda()[:, :p.K], p.b.cuda()
                 C = torch.empty((p.M, p.N), dtype=A.dtype, device="cuda")
                 for _ in range(20):
                     gemm.matmul(A, B, C, stream=s)
@@ -68,11 +80,11 @@ def test_threads_with_their_own_streams():
 
 
 def test_cuda_graph_capture_and_replay():
-    probs = [inputs.make_problem("g0", "bf16", 768, 2560, 4096, seed_a=31, seed_b=32, dist_a="normal"),
+    probs = [inputs.make_problem("g0", "bf16", *SPLIT_SHAPES[0], seed_a=31, seed_b=32, dist_a="normal"),
              inputs.make_problem("g1", "tf32", 1000, 900, 700, seed_a=33, seed_b=34),
              inputs.make_problem("g2", "f16", 300, 520, 200, layout=1, seed_a=35, seed_b=36),
              # the pair on the transposed product with a split tail (row-major B)
-             inputs.make_problem("g3", "bf16", 1280, 1024, 4096, seed_a=37, seed_b=38, dist_a="normal")]
+             inputs.make_problem("g3", "bf16", *SPLIT_SHAPES[1], seed_a=37, seed_b=38, dist_a="normal")]
     s = torch.cuda.Stream()
     dev = [(p.a.cuda(), p.b.cuda(), torch.empty((p.M, p.N), dtype=TORCH[p.dtype], device="cuda")) for p in probs]
     with torch.cuda.stream(s):  # first calls outside capture: the stream's scratch is allocated here
