@@ -831,6 +831,34 @@ __device__ __forceinline__ void for_each_acc_chunk(uint32_t taddr, int nchunks, 
   }
 }
 
+// for_each_acc_chunk over the chunks first, first + step, ... of a warp's
+// accumulator rows (the single-CTA kernel's two sets of epilogue warps take
+// alternate chunks). Warp-collective.
+template <typename Use>
+__device__ __forceinline__ void for_each_acc_chunk_strided(uint32_t taddr, int nchunks, int first, int step, Use use) {
+  if (first >= nchunks) return;
+  uint32_t ra[32], rb[32];
+  __syncwarp();
+  tmem_ld_32x32b_x32(taddr + first * 32, ra);
+  tmem_wait_ld_into(ra);
+#pragma unroll 1
+  for (int c = first; c < nchunks; c += 2 * step) {
+    const int c1 = c + step, c2 = c + 2 * step;
+    __syncwarp();
+    if (c1 < nchunks) tmem_ld_32x32b_x32(taddr + c1 * 32, rb);
+    use(c, ra);
+    __syncwarp();
+    tmem_wait_ld_into(rb);
+    if (c1 < nchunks) {
+      __syncwarp();
+      if (c2 < nchunks) tmem_ld_32x32b_x32(taddr + c2 * 32, ra);
+      use(c1, rb);
+      __syncwarp();
+      tmem_wait_ld_into(ra);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 // FUSED = false: built for launches without a fused epilogue (p.fused == 0),
 // with that code left out.
@@ -863,6 +891,13 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = threadIdx.x & 31;
   const bool has_copy = !(p.a_tma && p.b_tma);
   const uint32_t full_count = 1u + (has_copy ? 4u : 0u);
+  // Warps 0-3 drain the accumulator; for tiles of four or more 32-column
+  // chunks, where TMA loads every operand and the launch has warps 6-9 (the
+  // copy warps' slots), those are a second set of epilogue warps taking every
+  // other chunk. (Narrower tiles keep the plain epilogue: with the second set
+  // in their code, 512^3 and 1024^3 ran 2% slower.)
+  constexpr bool kTwoSets = BN >= 128;
+  const int epi_warps = (kTwoSets && !has_copy && blockDim.x >= 320) ? 8 : 4;
 
   if (warp == 4 && lane == 0) {
     for (int s = 0; s < S; ++s) {
@@ -871,7 +906,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
-      mbar_init(acce0 + 8 * b, 4);
+      mbar_init(acce0 + 8 * b, epi_warps);
     }
     mbar_init(drain_bar, 1);
     *issued_slot = 0;
@@ -976,10 +1011,18 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(drain_bar);
       wait_phase_drain(p, drain_bar, 0);
     }
-  } else if (warp < 4) {
+  } else if (warp < 4 || (kTwoSets && epi_warps == 8)) {
     // ---------------------------------------------------------------- epilogue
+    // epilogue warp e (0..epi_warps-1) reads tensor-memory lane quadrant q
+    // (warp w may access lanes 32 * (w % 4) ..) and takes chunks set, set +
+    // nsets, ...; its ring of staging tiles is its share of the staging area
+    const int e = kTwoSets ? (warp < 4 ? warp : warp - 2) : warp;
+    const int q = kTwoSets ? (warp & 3) : warp;
+    const int set = kTwoSets ? (warp < 4 ? 0 : 1) : 0;
+    const int nsets = kTwoSets ? epi_warps / 4 : 1;
+    const int bufs = (kTwoSets && epi_warps == 8) ? (Cf::EPI_BUFS >= 2 ? Cf::EPI_BUFS / 2 : 1) : Cf::EPI_BUFS;
     int tc = 0;
-    EpiRing ring{sE + static_cast<uint32_t>(warp * Cf::EPI_BUFS * EPI_WARP_BYTES), Cf::EPI_BUFS, 0,
+    EpiRing ring{sE + static_cast<uint32_t>(e * bufs * EPI_WARP_BYTES), bufs, 0,
                  sE + static_cast<uint32_t>(Cf::EPI_BUFS * EPI_BYTES)};
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tc) {
       int mb, nb, bz;
@@ -988,13 +1031,17 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t use = (tc >> 1) & 1;
       if (!warp_wait_phase(p, accf0 + 8 * b, use, ROLE_EPILOGUE | (b << 8))) break;
       tc_fence_after();
-      const int row0 = mb * Cf::BM + warp * 32;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + b * Cf::ACC_COLS;
+      const int row0 = mb * Cf::BM + q * 32;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * Cf::ACC_COLS;
       int ncols = min(Cf::BN, p.N - nb * Cf::BN);
       if (!in_range(p, b * Cf::ACC_COLS + ((ncols + 31) / 32) * 32 <= Cf::TMEM_COLS, CHECK_TMEM_LD)) ncols = 0;
-      for_each_acc_chunk(taddr, (ncols + 31) / 32, [&](int c, const uint32_t(&r)[32]) {
+      auto emit = [&](int c, const uint32_t(&r)[32]) {
         emit_chunk<KindTraits<KIND>::out, FUSED>(p, &tmC, ring, lane, row0, nb * Cf::BN + c * 32, bz, r);
-      });
+      };
+      if constexpr (kTwoSets)
+        for_each_acc_chunk_strided(taddr, (ncols + 31) / 32, set, nsets, emit);
+      else
+        for_each_acc_chunk(taddr, (ncols + 31) / 32, emit);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * b);
