@@ -87,6 +87,29 @@ def test_tf32_2048_row_major_b_avoids_the_single_cta_kernel():
     assert gemm.plan_query("tf32", 2048, 2048, 2048)["kernel"] in (PAIR, TWO_PAIRS)
 
 
+def test_two_pairs_only_where_their_clusters_fit_whole_rounds():
+    """Clusters of two pairs cost about 1.2 us more per launch than single
+    pairs with the same rounds (BF16 3072^3: 35.2 against 34.1 us on GB300;
+    2048 x 2048 x 8192: 44.5 against 43.2); at 6144^3 with K-major B their 36
+    clusters fill eight whole rounds and they were faster (242.8 against
+    250.3 us)."""
+    assert gemm.plan_query("bf16", 3072, 3072, 3072)["kernel"] == PAIR
+    assert gemm.plan_query("bf16", 2048, 2048, 8192)["kernel"] == PAIR
+    assert gemm.plan_query("tf32", 2048, 2048, 2048)["kernel"] == PAIR
+    assert gemm.plan_query("bf16", 6144, 6144, 6144, layout=gemm.GEMM_B_K_MAJOR)["kernel"] == TWO_PAIRS
+
+
+def test_short_tails_stay_unsplit():
+    """Splitting the last round costs about 4 us per segment (partials out
+    and back): TF32 2560^3 ran 55.6 us split in three against 48.8 unsplit on
+    192-wide tiles; BF16 12288 x 4096 x 4096 with K-major B 237.5 split in
+    four against 221.3 unsplit on 224-wide tiles."""
+    p = gemm.plan_query("tf32", 2560, 2560, 2560)
+    assert (p["kernel"], p["tile_n"], p["tail_segs"]) == (PAIR_ON_CT, 192, 1)
+    p = gemm.plan_query("bf16", 12288, 4096, 4096, layout=gemm.GEMM_B_K_MAJOR)
+    assert (p["kernel"], p["tile_n"], p["tail_segs"]) == (PAIR, 224, 1)
+
+
 def test_tuning_hook_forces_the_plan():
     gemm.set_tuning(4, 256, 0, 0)
     try:
