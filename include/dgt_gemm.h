@@ -217,6 +217,11 @@ int gemm_e5m2_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, co
  * behind its host application, or a latency-bound path that cannot take the
  * synchronisation a cudaFree implies.
  *
+ * Nor does it pack operands: A or B rows that TMA cannot address in place are
+ * read by the kernel's copy warps (same results; the 4000 x 4100 x 4104 BF16
+ * product with 8200-byte rows took 363 us this way against 96 us through
+ * gemm_bf16, which packs them).
+ *
  * Limit: the array holds 16 MiB of fp32 partial tiles (64 split work items of
  * 256 KiB, plus their counters). A shape whose plan needs more is refused with
  * GEMM_ERR_SCRATCH_LIMIT and nothing is launched; shapes that split nothing
