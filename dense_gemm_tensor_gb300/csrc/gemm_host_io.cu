@@ -48,7 +48,7 @@ struct HostIo {
 };
 
 std::mutex g_mu;
-std::unordered_map<uint64_t, HostIo*> g_io;  // (device, stream) -> state; kept until gemm_free_host_buffers
+std::unordered_map<uint64_t, HostIo*> g_io;  // (device, stream) -> state; kept until gemm_free_workspaces
 
 HostIo* state_for(int dev, cudaStream_t stream) {
   const uint64_t key = (uint64_t(uint32_t(dev)) << 56) ^ uint64_t(reinterpret_cast<uintptr_t>(stream));
@@ -68,6 +68,22 @@ bool init_state(HostIo& s) {
          cudaEventCreateWithFlags(&s.computed[i], cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; ok && i < 2; ++i) ok = cudaEventCreateWithFlags(&s.slot[i].free, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
+    // release what was created, so that a later call starts again from nothing
+    cudaGetLastError();
+    if (s.in) cudaStreamDestroy(s.in);
+    if (s.out) cudaStreamDestroy(s.out);
+    if (s.done) cudaEventDestroy(s.done);
+    for (int i = 0; i < kMaxBlocks; ++i) {
+      if (s.arrived[i]) cudaEventDestroy(s.arrived[i]);
+      if (s.computed[i]) cudaEventDestroy(s.computed[i]);
+      s.arrived[i] = s.computed[i] = nullptr;
+    }
+    for (int i = 0; i < 2; ++i) {
+      if (s.slot[i].free) cudaEventDestroy(s.slot[i].free);
+      s.slot[i].free = nullptr;
+    }
+    s.in = s.out = nullptr;
+    s.done = nullptr;
     cudaGetLastError();
     return false;
   }
